@@ -1,0 +1,179 @@
+/*
+ * pwsgemm.h -- C ABI of the pipelined, warp-specialized GEMM library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Two products, both "a tiled matrix multiply whose K loop is software
+ * pipelined" as the Croqtile tutorial ch.6 ("同步：流水线、事件与双缓冲")
+ * builds it:
+ *
+ *   gemm_s32_nn  -- the s32 kernel of section "使用 swap 的双缓冲": a
+ *                   two-buffer ring filled by asynchronous copies, with a
+ *                   prologue load, steady iterations (load tile t, compute
+ *                   tile t-1, swap the buffer names) and an epilogue compute.
+ *                   Runs on the CUDA cores (wrapping 32-bit multiply-add).
+ *   gemm_f16_nt  -- the f16 kernel of section "带 event 的 1P1C 内核": a
+ *                   producer role fills an S-slot shared-memory ring guarded
+ *                   by full[s]/empty[s] events (stage = k % S, every empty
+ *                   seeded before the loop); a consumer role multiplies on
+ *                   the tensor cores and releases each slot once its
+ *                   multiply has completed ("mma.commit"), then writes the
+ *                   output tile.  Accumulates in fp32, stores f16.
+ *
+ * Conventions shared by every entry point:
+ *   - Matrices are dense and row-major, in DEVICE memory of the current CUDA
+ *     device, owned by the caller.  `out` must not overlap `lhs` or `rhs`.
+ *   - Calls are asynchronous and stream-ordered on `stream` (0 = the legacy
+ *     default stream).  They do not synchronize and do not allocate device
+ *     memory per call.
+ *   - Argument errors are reported by the return value BEFORE any launch;
+ *     nothing is written in that case.
+ *   - M == 0 or N == 0 is a successful no-op.  K == 0 writes zeros to `out`
+ *     (the empty sum).
+ *   - A wait inside a kernel that exceeds the wait limit (see
+ *     gemm_set_wait_timeout_ns) records GEMM_ERR_TIMEOUT in a device status
+ *     word and the kernel returns; gemm_device_status() reads and clears it.
+ */
+#ifndef PWSGEMM_H_
+#define PWSGEMM_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* negative size, null pointer, overlap, size too large */
+    GEMM_ERR_ALIGNMENT = 2,          /* pointer not aligned to its element size               */
+    GEMM_ERR_UNSUPPORTED_STAGES = 3, /* stages outside 1..6                                   */
+    GEMM_ERR_UNSUPPORTED_ARCH = 4,   /* current device is not compute capability 10.3        */
+    GEMM_ERR_LAUNCH = 5,             /* CUDA runtime or driver call failed                    */
+    GEMM_ERR_TIMEOUT = 6             /* a bounded device wait expired (see gemm_device_status)*/
+} gemm_status;
+
+/* Binary16 values are passed as their IEEE 754 bit patterns. */
+typedef uint16_t gemm_f16_t;
+
+/*
+ * gemm_s32_nn -- out[M,N] = lhs[M,K] . rhs[K,N] over int32.
+ *
+ * Croqtile tutorial ch.6, section "使用 swap 的双缓冲" (the s32 matmul with
+ * "with tile_k in 16", "foreach tile_k(1:)" and swap(lf0, lf1)).
+ *
+ *   lhs : int32 [M, K], row-major (row stride K elements), 4-byte aligned
+ *   rhs : int32 [K, N], row-major (row stride N elements), 4-byte aligned
+ *   out : int32 [M, N], row-major, written (not accumulated into)
+ *
+ * The sum of products is computed with wrapping 32-bit arithmetic (two's
+ * complement, i.e. the exact sum modulo 2^32).  K is cut into tiles of 16;
+ * a partial last tile and partial edge tiles are zero-filled.
+ *
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (M, N or K negative, a null pointer
+ * with M*N > 0, or out overlapping an input), GEMM_ERR_ALIGNMENT (a pointer not
+ * 4-byte aligned), GEMM_ERR_UNSUPPORTED_ARCH or GEMM_ERR_LAUNCH.
+ */
+int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32_t* rhs,
+                int32_t* out, cudaStream_t stream);
+
+/*
+ * gemm_f16_nt -- out[M,N] = f16( lhs[M,K] . rhs[N,K]^T ), fp32 accumulation.
+ *
+ * Croqtile tutorial ch.6, section "带 event 的 1P1C 内核" (lhs declared
+ * [M, K], rhs declared [N, K], multiplied with mma.row.row: C = A . B^T),
+ * with the ring index of section "环形索引" and the seeding of "消费者路径";
+ * the phase bit of each reused event follows TileLang tutorial ch.22,
+ * section 3.2 (parity = (k / S) mod 2).
+ *
+ *   lhs    : binary16 [M, K], row-major (row stride K elements), 2-byte aligned
+ *   rhs    : binary16 [N, K], row-major (row stride K elements), 2-byte aligned
+ *   out    : binary16 [M, N], row-major, written; each element is the fp32 sum
+ *            rounded to nearest-even binary16 (overflow gives +-inf)
+ *   stages : S, the number of shared-memory ring slots, 1..6.  S = 1 is the
+ *            single-buffer case (load and multiply serialise).  The result is
+ *            bitwise identical for every S.
+ *
+ * The producer uses the tensor memory accelerator when both operands start
+ * on 16-byte boundaries and K is a multiple of 8 (row stride a multiple of 16
+ * bytes); otherwise an asynchronous-copy producer fills the same swizzled
+ * ring.  Partial tiles are zero-filled on load and clipped on store.
+ *
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT (a pointer not
+ * 2-byte aligned), GEMM_ERR_UNSUPPORTED_STAGES, GEMM_ERR_UNSUPPORTED_ARCH or
+ * GEMM_ERR_LAUNCH.  M, N, K must each be below 2^31.
+ */
+int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
+                gemm_f16_t* out, int stages, cudaStream_t stream);
+
+/*
+ * gemm_device_status -- synchronizes `stream`, then returns and clears the
+ * device status word of the current device: GEMM_OK, or GEMM_ERR_TIMEOUT if a
+ * bounded wait inside any kernel of this library expired since the last call.
+ * Returns GEMM_ERR_LAUNCH if the synchronization itself failed.
+ *
+ * Every device-side wait of the pipelines (mbarrier phase waits) gives up
+ * after the wait limit; the waiting role then records the timeout, drains
+ * what it has in flight and the kernel returns, so the CUDA context stays
+ * usable.  This is the device analogue of the deadlock the Croqtile tutorial
+ * ch.6 describes for a missing empty seed ("消费者路径").
+ */
+int gemm_device_status(cudaStream_t stream);
+
+/* gemm_status_string -- a static, human-readable name for a status code. */
+const char* gemm_status_string(int status);
+
+/*
+ * gemm_set_wait_timeout_ns -- sets the limit of every bounded device wait
+ * for later launches (default 2e9 ns = 2 s; 0 restores the default).  Host
+ * state only; returns GEMM_OK.
+ */
+int gemm_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Debug flags for later launches (host state only; 0 = normal operation).
+ *   GEMM_DEBUG_SKIP_EMPTY_SEED     : the consumer does not seed the empty
+ *       events (Croqtile ch.6, "消费者路径": the producer's first wait then
+ *       never completes); used to test that the bounded waits turn this
+ *       deadlock into GEMM_ERR_TIMEOUT.
+ *   GEMM_DEBUG_FORCE_COPY_PRODUCER : use the asynchronous-copy producer even
+ *       where the tensor memory accelerator could be used.
+ *   GEMM_DEBUG_FORCE_DIRECT_STORE  : store the output with guarded plain
+ *       stores instead of the tensor memory accelerator.
+ *   GEMM_DEBUG_FORCE_SOLO_TILE     : use the one-CTA 128x128 tile even where
+ *       the CTA-pair 256x256 tile would be chosen.
+ *   GEMM_DEBUG_FORCE_PAIR_TILE     : use the CTA-pair 256x256 tile whenever the
+ *       TMA producer is used, even for small outputs.
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
+ */
+enum {
+    GEMM_DEBUG_SKIP_EMPTY_SEED = 1u,
+    GEMM_DEBUG_FORCE_COPY_PRODUCER = 2u,
+    GEMM_DEBUG_FORCE_DIRECT_STORE = 4u,
+    GEMM_DEBUG_FORCE_SOLO_TILE = 8u,
+    GEMM_DEBUG_FORCE_PAIR_TILE = 16u
+};
+int gemm_set_debug_flags(unsigned flags);
+
+/*
+ * gemm_f16_nt_plan -- the launch plan gemm_f16_nt would use for these
+ * arguments, without touching a device (host logic only).  Validates the
+ * arguments exactly as gemm_f16_nt does and returns the same status.
+ *   plan[0] tile rows per CTA group (BM)      plan[1] tile columns (BN)
+ *   plan[2] K per ring slot (BK)              plan[3] CTAs per tile (1 or 2)
+ *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy
+ *   plan[5] copy granularity in bytes (16 for TMA, else 8, 4 or 2)
+ *   plan[6] output store: 0 = tensor memory accelerator, 1 = plain stores
+ *   plan[7] dynamic shared memory bytes per CTA
+ *   plan[8] number of output tiles        plan[9] number of K blocks
+ * `plan` must hold 10 int64 values.
+ */
+int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
+                     const gemm_f16_t* out, int stages, int64_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PWSGEMM_H_ */

@@ -1,0 +1,722 @@
+// gemm_f16_nt.cu -- out[M,N] = f16( lhs[M,K] . rhs[N,K]^T ) on the 5th-generation
+// tensor cores of sm_103a.
+//
+// The pipeline is the 1P1C kernel of the Croqtile tutorial ch.6, section
+// "带 event 的 1P1C 内核", re-built for tcgen05/TMEM/TMA:
+//
+//   * ring      -- S shared-memory slots, each holding one 64-wide K strip of
+//                  the A tile and of the B tile, laid out in the 128-byte
+//                  swizzle that both the TMA and the tensor-core descriptors
+//                  use.  Slot for K block k is stage = k % S ("环形索引").
+//   * events    -- full[s] / empty[s] mbarriers, one pair per slot.  full[s]
+//                  counts the transaction bytes of the slot's copies
+//                  (expect-tx), empty[s] is arrived by the tensor-core
+//                  commit.  Lap l of a slot is waited with parity l mod 2
+//                  (TileLang tutorial ch.22, section 3.2).
+//   * producer  -- one warp (one elected thread) issues the TMA copies:
+//                  wait empty[s], arm full[s] with the byte count, copy A and
+//                  B strips into slot s.  Where TMA cannot address the
+//                  operands (rows not 16-byte aligned), four warps fill the
+//                  same swizzled layout with cp.async and arrive on full[s]
+//                  once their copies have landed and been fenced to the async
+//                  proxy (CUDA tutorial ch.4, section 4.8.1).
+//   * consumer  -- one warp (one elected thread) seeds every empty[s] once
+//                  before its loop ("foreach {s} in [MATMUL_STAGES] trigger
+//                  empty[s]"), then per K block waits full[s], issues four
+//                  tcgen05.mma (K = 16 each) into an fp32 accumulator in
+//                  tensor memory, and commits to empty[s] -- the commit is
+//                  the "mma.commit" fence: the slot is released only once the
+//                  multiplies reading it have completed.
+//   * epilogue  -- four warps, one per 32-lane quarter of tensor memory,
+//                  wait for the accumulator, read it with tcgen05.ld, round to
+//                  f16 (nearest even), stage 32 x 64 blocks in swizzled shared
+//                  memory and store them with TMA (clipped at M and N), or
+//                  with guarded plain stores where TMA cannot address `out`.
+//
+// The kernel is persistent (the Croqtile tutorial ch.5 "持久调度与 if 守卫"):
+// a fixed grid strides over output tiles, and the accumulator is double
+// buffered in tensor memory so the epilogue of tile i overlaps the main loop
+// of tile i+1 (two more event pairs, tmem_full[2] / tmem_empty[2], seeded by
+// the epilogue warps the same way).
+//
+// Two tile shapes share the code: a CTA pair (cta_group::2, 256 x 256 per
+// pair, each CTA loading its own 128 rows of A and 128 rows of B -- no
+// multicast) and a single CTA (128 x 128).  Every ring slot is 32 KB per CTA
+// in both, so S = 1..6 fit the shared memory with the epilogue staging, and
+// for a fixed shape the tile configuration does not depend on S.
+//
+// Every wait is bounded (wait_timeout_ns); a role that gives up records a
+// timeout in the library's status word, raises a CTA-local abort flag that
+// the other roles poll, and every role then runs the common exit path, so
+// the kernel always returns.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "pwsgemm.h"
+
+namespace pws {
+namespace f16nt {
+
+constexpr int BK = 64;                 // K per ring slot: 64 f16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;             // K per tcgen05.mma of kind::f16
+constexpr int BM_CTA = 128;            // A rows per CTA (tensor-memory lanes)
+constexpr int BN_CTA = 128;            // B rows per CTA
+constexpr int A_SLOT = BM_CTA * BK * 2;
+constexpr int B_SLOT = BN_CTA * BK * 2;
+constexpr int SLOT_BYTES = A_SLOT + B_SLOT;   // 32 KB
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128 bytes of f16)
+constexpr int EPI_BUF = 32 * EPI_COLS * 2;     // 32 rows x 64 columns
+constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+constexpr int MAX_STAGES = 6;
+constexpr int COPY_WARPS = 4;          // producer warps of the cp.async producer
+constexpr int GROUP_M = 8;             // tile-row group height of the raster order
+
+enum { kProducerTma = 0, kProducerCopy = 1 };
+enum { kStoreTma = 0, kStoreDirect = 1 };
+
+struct Params {
+    int M, N, K;
+    int num_kb;                 // K blocks: cdiv(K, BK)
+    int tiles_m, tiles_n, num_tiles;
+    int producer;               // kProducerTma / kProducerCopy
+    int copy_bytes;             // cp.async granularity (8, 4) or 2 (plain loads)
+    int store;                  // kStoreTma / kStoreDirect
+    unsigned flags;             // GEMM_DEBUG_* bits
+    unsigned long long timeout_ns;
+    const __half* lhs;
+    const __half* rhs;
+    __half* out;
+    unsigned* status;
+};
+
+template <int CG>
+struct Shape {
+    static constexpr int UMMA_M = BM_CTA * CG;        // tile rows (per CTA group)
+    static constexpr int UMMA_N = BN_CTA * CG;        // tile columns
+    static constexpr int ACC_COLS = UMMA_N;           // fp32 columns per accumulator
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;    // double-buffered accumulator
+};
+
+// Shared-memory carve-up (offsets from a 1024-byte aligned base).
+template <int S>
+struct Layout {
+    static constexpr int A = 0;
+    static constexpr int B = S * A_SLOT;
+    static constexpr int EPI = S * SLOT_BYTES;
+    static constexpr int BAR = EPI + EPI_BYTES;
+    static constexpr int FULL = BAR;
+    static constexpr int EMPTY = FULL + 8 * S;
+    static constexpr int TFULL = EMPTY + 8 * S;
+    static constexpr int TEMPTY = TFULL + 16;
+    static constexpr int DRAIN = TEMPTY + 16;
+    static constexpr int TMEM_SLOT = DRAIN + 8;
+    static constexpr int ABORT = TMEM_SLOT + 4;
+    static constexpr int END = ABORT + 4;
+    static constexpr int BYTES = END + 1024;                // + alignment slack
+    // at least ~half the SM's shared memory so only one CTA is resident per SM
+    // (each CTA owns up to all 512 tensor-memory columns)
+    static constexpr int DYN = BYTES > 120 * 1024 ? BYTES : 120 * 1024;
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B f16, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+template <int M_, int N_>
+constexpr uint32_t make_idesc() {
+    return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
+           (static_cast<uint32_t>(N_ >> 3) << 17) | (static_cast<uint32_t>(M_ >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle: rows of 128 bytes, 8-row atoms of 1024 bytes (stride-dimension
+// offset), start address >> 4 in bits 0..13, descriptor version 1 at bit 46,
+// layout "128-byte swizzle" (2) at bit 61.  Advancing K by 16 elements moves
+// the start address by 32 bytes inside the swizzle row.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16u >> 4) << 16;     // leading-dimension offset (unused here)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;   // stride-dimension offset: 8 rows x 128 B
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Output tile of persistent work item `t`: tile rows are grouped GROUP_M at a
+// time so the CTAs working at the same moment share A and B strips in L2.
+__device__ __forceinline__ void tile_coords(int t, const Params& p, int& tm, int& tn) {
+    const int group = GROUP_M * p.tiles_n;
+    const int g = t / group;
+    const int first = g * GROUP_M;
+    const int rows = min(p.tiles_m - first, GROUP_M);
+    const int r = t - g * group;
+    tm = first + r % rows;
+    tn = r / rows;
+}
+
+// Bounded mbarrier wait.  Returns false if the wait gave up (time limit or
+// another role's abort); the first role to give up records the timeout.
+struct Waiter {
+    unsigned long long timeout_ns;
+    volatile uint32_t* abort;
+    unsigned* status;
+    unsigned role;
+
+    template <bool CLUSTER_SCOPE = false>
+    __device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) const {
+        return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    }
+
+    template <bool CLUSTER_SCOPE = false>
+    __device__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                *abort = 1u;
+                atomicOr(status, kStatusTimeout | role);
+                return false;
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int CG, int S>
+__global__ void __launch_bounds__((COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
+gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
+    using SH = Shape<CG>;
+    using L = Layout<S>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (base - raw);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int P = static_cast<int>(blockDim.x / 32) - 1 - EPI_WARPS;   // producer warps
+    const int mma_warp = P;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int cluster_id = blockIdx.x / CG;
+    const int num_clusters = gridDim.x / CG;
+
+    const uint32_t sA = base + L::A, sB = base + L::B, sEPI = base + L::EPI;
+    const uint32_t bFULL = base + L::FULL, bEMPTY = base + L::EMPTY;
+    const uint32_t bTFULL = base + L::TFULL, bTEMPTY = base + L::TEMPTY, bDRAIN = base + L::DRAIN;
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L::ABORT);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::TMEM_SLOT);
+
+    // ------------------------------------------------------------ set-up
+    if (threadIdx.x == 0) {
+        const uint32_t full_count = p.producer == kProducerTma ? 1u : static_cast<uint32_t>(P * 32);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bFULL + 8 * s, full_count);
+            mbar_init(bEMPTY + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bTFULL + 8 * b, 1);
+            mbar_init(bTEMPTY + 8 * b, EPI_WARPS * CG);
+        }
+        mbar_init(bDRAIN, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0 && p.producer == kProducerTma) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (p.store == kStoreTma) tma_prefetch_desc(&tmC);
+    }
+    if (warp == mma_warp) {
+        tmem_alloc<CG>(base + L::TMEM_SLOT, SH::TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const bool is_leader = (CG == 1) || rank == 0;
+
+    if (warp < P) {
+        // ======================================================== producer
+        if (p.producer == kProducerTma) {
+            if (lane == 0) {
+                const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
+                // the slot's full barrier lives in the leader CTA of a pair
+                const uint32_t full_leader = (CG == 2) ? mapa_shared(bFULL, 0) : bFULL;
+                uint32_t stage = 0, phase = 0;
+                uint32_t issued = 0;
+                bool ok = true;
+                for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                    int tm, tn;
+                    tile_coords(t, p, tm, tn);
+                    const int m_cta = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA;
+                    const int n_cta = tn * SH::UMMA_N + static_cast<int>(rank) * BN_CTA;
+                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                        if (!W.wait(bEMPTY + 8 * stage, phase)) { ok = false; break; }
+                        const uint32_t a_dst = sA + stage * A_SLOT, b_dst = sB + stage * B_SLOT;
+                        if constexpr (CG == 1) {
+                            mbar_arrive_expect_tx(bFULL + 8 * stage, SLOT_BYTES);
+                            tma_load_2d(a_dst, &tmA, kb * BK, m_cta, bFULL + 8 * stage);
+                            tma_load_2d(b_dst, &tmB, kb * BK, n_cta, bFULL + 8 * stage);
+                        } else {
+                            // the leader arms its barrier for the bytes of both CTAs
+                            if (rank == 0) mbar_arrive_expect_tx(bFULL + 8 * stage, 2 * SLOT_BYTES);
+                            tma_load_2d_pair(a_dst, &tmA, kb * BK, m_cta, full_leader + 8 * stage);
+                            tma_load_2d_pair(b_dst, &tmB, kb * BK, n_cta, full_leader + 8 * stage);
+                        }
+                        ++issued;
+                        if (++stage == S) { stage = 0; phase ^= 1u; }
+                    }
+                }
+                if (!ok && is_leader) {
+                    // drain: wait (bounded) for the copies still in flight into this CTA
+                    const Waiter D{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
+                    volatile uint32_t no_abort = 0;
+                    const Waiter Dn{D.timeout_ns, &no_abort, D.status, D.role};
+                    const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+                    for (uint32_t it = first; it < issued; ++it)
+                        if (!Dn.wait(bFULL + 8 * (it % S), (it / S) & 1u)) break;
+                }
+            }
+        } else if constexpr (CG == 1) {
+            // cp.async producer (single CTA only): P warps fill the swizzled slot
+            const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
+            const int ptid = threadIdx.x;                 // 0 .. P*32-1
+            const int nthr = P * 32;
+            const int G = p.copy_bytes;                  // bytes per copy
+            const int E = G / 2;                         // f16 per copy
+            const int per_row = BK / E;
+            uint32_t stage = 0, phase = 0;
+            int prev = -1;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                int tm, tn;
+                tile_coords(t, p, tm, tn);
+                const int m_cta = tm * SH::UMMA_M;
+                const int n_cta = tn * SH::UMMA_N;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    bool got = true;
+                    if (lane == 0) got = W.wait(bEMPTY + 8 * stage, phase);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) { ok = false; break; }
+                    const int k0 = kb * BK;
+                    for (int op = 0; op < 2; ++op) {
+                        const __half* src_base = op == 0 ? p.lhs : p.rhs;
+                        const int rows_total = op == 0 ? p.M : p.N;
+                        const int row0 = op == 0 ? m_cta : n_cta;
+                        const uint32_t dst_base = (op == 0 ? sA + stage * A_SLOT : sB + stage * B_SLOT);
+                        for (int i = ptid; i < BM_CTA * per_row; i += nthr) {
+                            const int r = i / per_row;
+                            const int c = (i - r * per_row) * E;        // f16 column inside the strip
+                            const int gr = row0 + r, gk = k0 + c;
+                            const bool valid = gr < rows_total && gk < p.K;
+                            const uint32_t bo = static_cast<uint32_t>(c * 2);
+                            const uint32_t dst = dst_base + r * 128 +
+                                                 ((((bo >> 4) ^ static_cast<uint32_t>(r & 7)) << 4) | (bo & 15u));
+                            const __half* src = valid ? src_base + static_cast<int64_t>(gr) * p.K + gk : src_base;
+                            if (G == 8) {
+                                cp_async<8>(dst, src, valid ? 8u : 0u);
+                            } else if (G == 4) {
+                                cp_async<4>(dst, src, valid ? 4u : 0u);
+                            } else {
+                                const unsigned short v =
+                                    valid ? __ldg(reinterpret_cast<const unsigned short*>(src)) : (unsigned short)0;
+                                asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst), "h"(v) : "memory");
+                            }
+                        }
+                    }
+                    cp_async_commit();
+                    if (S > 1) {
+                        // signal the previous slot once its copies have landed
+                        if (prev >= 0) {
+                            cp_async_wait_group<1>();
+                            fence_proxy_async_smem();
+                            mbar_arrive(bFULL + 8 * prev);
+                        }
+                        prev = static_cast<int>(stage);
+                    } else {
+                        cp_async_wait_group<0>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(bFULL + 8 * stage);
+                    }
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            cp_async_wait_group<0>();
+            if (ok && S > 1 && prev >= 0) {
+                fence_proxy_async_smem();
+                mbar_arrive(bFULL + 8 * prev);
+            }
+        }
+        __syncwarp();
+    } else if (warp == mma_warp) {
+        // ======================================================== MMA issuer
+        if (lane == 0) {
+            // seed: every slot starts with one empty credit
+            if (!(p.flags & GEMM_DEBUG_SKIP_EMPTY_SEED))
+                for (int s = 0; s < S; ++s) mbar_arrive(bEMPTY + 8 * s);
+        }
+        if (is_leader && lane == 0) {
+            const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleMma};
+            constexpr uint32_t IDESC = make_idesc<SH::UMMA_M, SH::UMMA_N>();
+            uint32_t stage = 0, phase = 0;
+            uint32_t tcount = 0;
+            bool ok = true, issued_any = false;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tcount) {
+                const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
+                if (!W.template wait<CG == 2>(bTEMPTY + 8 * b, aph)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * SH::ACC_COLS;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!W.wait(bFULL + 8 * stage, phase)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    if (p.producer == kProducerCopy) fence_proxy_async_smem();
+                    const uint64_t adesc = make_sdesc(sA + stage * A_SLOT);
+                    const uint64_t bdesc = make_sdesc(sB + stage * B_SLOT);
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // +32 bytes of K per step: +2 in the (address >> 4) field
+                        tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+                    }
+                    issued_any = true;
+                    // release the slot once these multiplies have read it
+                    if constexpr (CG == 1) tc_commit_1(bEMPTY + 8 * stage);
+                    else tc_commit_2_mc(bEMPTY + 8 * stage, 0x3);
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                // accumulator of this tile is complete
+                if constexpr (CG == 1) tc_commit_1(bTFULL + 8 * b);
+                else tc_commit_2_mc(bTFULL + 8 * b, 0x3);
+            }
+            if (issued_any) {
+                // all multiplies have finished before tensor memory is released
+                if constexpr (CG == 1) tc_commit_1(bDRAIN);
+                else tc_commit_2_mc(bDRAIN, 0x1);
+                volatile uint32_t no_abort = 0;
+                const Waiter D{p.timeout_ns, &no_abort, p.status, kStatusRoleMma};
+                D.wait(bDRAIN, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ======================================================== epilogue
+        const int e = warp - P - 1;              // 0..3
+        const int q = warp & 3;                  // tensor-memory lane quarter of this warp
+        const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleEpilogue};
+        const uint32_t tempty_leader = (CG == 2) ? mapa_shared(bTEMPTY, 0) : bTEMPTY;
+        // seed: both accumulator buffers start free
+        if (lane == 0) {
+            for (int b = 0; b < 2; ++b) {
+                if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * b);
+                else mbar_arrive_cluster(tempty_leader + 8 * b);
+            }
+        }
+        uint32_t tcount = 0, sbuf = 0;
+        for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tcount) {
+            const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
+            bool got = true;
+            if (lane == 0) got = W.wait(bTFULL + 8 * b, aph);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) break;
+            tc_fence_after_sync();
+            int tm, tn;
+            tile_coords(t, p, tm, tn);
+            const int row0 = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA + q * 32;
+            for (int c = 0; c < SH::ACC_COLS / EPI_COLS; ++c) {
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * SH::ACC_COLS +
+                                       static_cast<uint32_t>(c * EPI_COLS);
+                tmem_ld_32x32b_x32(taddr, v0);
+                tmem_ld_32x32b_x32(taddr + 32, v1);
+                tmem_ld_wait();
+                uint32_t h[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h[i] = pack_half2(v0[2 * i], v0[2 * i + 1]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h[16 + i] = pack_half2(v1[2 * i], v1[2 * i + 1]);
+                const int col0 = tn * SH::UMMA_N + c * EPI_COLS;
+                if (p.store == kStoreTma) {
+                    const uint32_t buf = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF + sbuf * EPI_BUF;
+                    // the store issued from this buffer two chunks ago has finished reading it
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h[4 * j]),
+                                     "r"(h[4 * j + 1]), "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    // a box wholly past M or N (padding rows of a pair tile) is not stored
+                    if (lane == 0 && row0 < p.M && col0 < p.N) {
+                        tma_store_2d(&tmC, buf, col0, row0);
+                        bulk_commit_group();
+                    }
+                    sbuf ^= 1u;
+                } else {
+                    const int row = row0 + lane;
+                    if (row < p.M) {
+                        unsigned short* dst = reinterpret_cast<unsigned short*>(p.out) + static_cast<int64_t>(row) * p.N;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int col = col0 + 2 * i;
+                            if (col < p.N) dst[col] = static_cast<unsigned short>(h[i] & 0xFFFFu);
+                            if (col + 1 < p.N) dst[col + 1] = static_cast<unsigned short>(h[i] >> 16);
+                        }
+                    }
+                }
+            }
+            // this warp's reads of accumulator buffer b are complete
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * b);
+                else mbar_arrive_cluster(tempty_leader + 8 * b);
+            }
+        }
+        if (lane == 0 && p.store == kStoreTma) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ------------------------------------------------------------ tear-down
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (CG == 2) cluster_sync();
+    if (warp == mma_warp) {
+        tc_fence_after_sync();
+        tmem_dealloc<CG>(tmem_base, SH::TMEM_COLS);
+    }
+}
+
+// Fills a f16 [M,N] output with zeros (K == 0: the empty sum).
+__global__ void zero_fill_u16(unsigned short* out, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[i] = 0;
+}
+
+struct Plan {
+    int cg = 1;
+    int producer = kProducerTma;
+    int copy_bytes = 16;
+    int store = kStoreTma;
+    int tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0;
+    int smem = 0;
+};
+
+template <int S>
+constexpr int dyn_smem() { return Layout<S>::DYN; }
+
+int smem_for(int stages) {
+    switch (stages) {
+        case 1: return dyn_smem<1>();
+        case 2: return dyn_smem<2>();
+        case 3: return dyn_smem<3>();
+        case 4: return dyn_smem<4>();
+        case 5: return dyn_smem<5>();
+        default: return dyn_smem<6>();
+    }
+}
+
+// Argument checks shared by the plan query and the launch.
+int validate(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, const void* out, int stages) {
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
+    if (stages < 1 || stages > MAX_STAGES) return GEMM_ERR_UNSUPPORTED_STAGES;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!out || (K > 0 && (!lhs || !rhs))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lhs) | reinterpret_cast<uintptr_t>(rhs)) & 1u)
+        return GEMM_ERR_ALIGNMENT;
+    const uint64_t out_b = static_cast<uint64_t>(M) * N * 2;
+    if (K > 0 && (ranges_overlap(out, out_b, lhs, static_cast<uint64_t>(M) * K * 2) ||
+                  ranges_overlap(out, out_b, rhs, static_cast<uint64_t>(N) * K * 2)))
+        return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, const void* out, int stages,
+               int num_sms, unsigned flags) {
+    Plan pl;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(lhs), b = reinterpret_cast<uintptr_t>(rhs);
+    const uintptr_t o = reinterpret_cast<uintptr_t>(out);
+    const bool tma_ok = !(flags & GEMM_DEBUG_FORCE_COPY_PRODUCER) && K % 8 == 0 && a % 16 == 0 && b % 16 == 0;
+    if (tma_ok) {
+        pl.producer = kProducerTma;
+        pl.copy_bytes = 16;
+    } else {
+        pl.producer = kProducerCopy;
+        if (K % 4 == 0 && a % 8 == 0 && b % 8 == 0) pl.copy_bytes = 8;
+        else if (K % 2 == 0 && a % 4 == 0 && b % 4 == 0) pl.copy_bytes = 4;
+        else pl.copy_bytes = 2;
+    }
+    pl.store = (!(flags & GEMM_DEBUG_FORCE_DIRECT_STORE) && N % 8 == 0 && o % 16 == 0) ? kStoreTma : kStoreDirect;
+    // The CTA-pair tile when TMA feeds it and there are enough pair tiles to
+    // occupy the GPU; otherwise the single-CTA tile.
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    const bool want_pair = (flags & GEMM_DEBUG_FORCE_PAIR_TILE) || 2 * pair_tiles >= num_sms;
+    pl.cg = (pl.producer == kProducerTma && !(flags & GEMM_DEBUG_FORCE_SOLO_TILE) && want_pair) ? 2 : 1;
+    const int tile = 128 * pl.cg;
+    pl.tiles_m = static_cast<int>((M + tile - 1) / tile);
+    pl.tiles_n = static_cast<int>((N + tile - 1) / tile);
+    pl.num_tiles = pl.tiles_m * pl.tiles_n;
+    pl.num_kb = static_cast<int>((K + BK - 1) / BK);
+    pl.smem = smem_for(stages);
+    return pl;
+}
+
+template <int CG, int S>
+int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+           const Params& p, cudaStream_t stream) {
+    auto kern = gemm_f16_nt_kernel<CG, S>;
+    constexpr int smem = Layout<S>::DYN;
+    static_assert(Layout<S>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
+    static int configured[64] = {};
+    static int max_clusters[64] = {};
+    const int threads = ((pl.producer == kProducerTma ? 1 : COPY_WARPS) + 1 + EPI_WARPS) * 32;
+    if (!configured[info.device]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return GEMM_ERR_LAUNCH;
+        configured[info.device] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int grid_ctas;
+    if constexpr (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (!max_clusters[info.device]) {
+            int n = 0;
+            cfg.gridDim = dim3(2 * info.num_sms, 1, 1);
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = info.num_sms / 2;
+            }
+            max_clusters[info.device] = n;
+        }
+        const int clusters = pl.num_tiles < max_clusters[info.device] ? pl.num_tiles : max_clusters[info.device];
+        grid_ctas = 2 * clusters;
+    } else {
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        grid_ctas = pl.num_tiles < info.num_sms ? pl.num_tiles : info.num_sms;
+    }
+    cfg.gridDim = dim3(grid_ctas, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    return GEMM_OK;
+}
+
+template <int CG>
+int launch_stages(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
+                  const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
+    switch (stages) {
+        case 1: return launch<CG, 1>(pl, info, ta, tb, tc, p, stream);
+        case 2: return launch<CG, 2>(pl, info, ta, tb, tc, p, stream);
+        case 3: return launch<CG, 3>(pl, info, ta, tb, tc, p, stream);
+        case 4: return launch<CG, 4>(pl, info, ta, tb, tc, p, stream);
+        case 5: return launch<CG, 5>(pl, info, ta, tb, tc, p, stream);
+        case 6: return launch<CG, 6>(pl, info, ta, tb, tc, p, stream);
+        default: return GEMM_ERR_UNSUPPORTED_STAGES;
+    }
+}
+
+}  // namespace f16nt
+}  // namespace pws
+
+extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
+                                const gemm_f16_t* out, int stages, int64_t* plan) {
+    using namespace pws::f16nt;
+    const int rc = validate(M, N, K, lhs, rhs, out, stages);
+    if (rc != GEMM_OK) return rc;
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, pws::sm_count_or_default(), pws::debug_flags());
+    plan[0] = 128 * pl.cg;
+    plan[1] = 128 * pl.cg;
+    plan[2] = BK;
+    plan[3] = pl.cg;
+    plan[4] = pl.producer;
+    plan[5] = pl.copy_bytes;
+    plan[6] = pl.store;
+    plan[7] = pl.smem;
+    plan[8] = pl.num_tiles;
+    plan[9] = pl.num_kb;
+    return GEMM_OK;
+}
+
+extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
+                           gemm_f16_t* out, int stages, cudaStream_t stream) {
+    using namespace pws;
+    using namespace pws::f16nt;
+    int rc = validate(M, N, K, lhs, rhs, out, stages);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceInfo info;
+    rc = current_device(&info);
+    if (rc != GEMM_OK) return rc;
+    if (K == 0) {
+        const int64_t n = M * N;
+        int blocks = static_cast<int>((n + 255) / 256);
+        if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
+        zero_fill_u16<<<blocks, 256, 0, stream>>>(reinterpret_cast<unsigned short*>(out), n);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+    const unsigned flags = debug_flags();
+    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+
+    CUtensorMap ta, tb, tc;
+    memset(&ta, 0, sizeof(ta));
+    memset(&tb, 0, sizeof(tb));
+    memset(&tc, 0, sizeof(tc));
+    if (pl.producer == kProducerTma) {
+        if (!encode_tmap_f16_2d(&ta, lhs, K, M, K * 2, BK, BM_CTA) ||
+            !encode_tmap_f16_2d(&tb, rhs, K, N, K * 2, BK, BN_CTA))
+            return GEMM_ERR_LAUNCH;
+    }
+    if (pl.store == kStoreTma) {
+        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return GEMM_ERR_LAUNCH;
+    }
+    Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = pl.num_kb;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.num_tiles;
+    p.producer = pl.producer;
+    p.copy_bytes = pl.copy_bytes;
+    p.store = pl.store;
+    p.flags = flags;
+    p.timeout_ns = wait_timeout_ns();
+    p.lhs = reinterpret_cast<const __half*>(lhs);
+    p.rhs = reinterpret_cast<const __half*>(rhs);
+    p.out = reinterpret_cast<__half*>(out);
+    p.status = info.status;
+    if (pl.cg == 2) return launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream);
+    return launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream);
+}

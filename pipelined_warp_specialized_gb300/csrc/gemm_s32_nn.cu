@@ -1,0 +1,180 @@
+// gemm_s32_nn.cu -- out[M,N] = lhs[M,K] . rhs[K,N] over int32 on the CUDA cores.
+//
+// The schedule is the two-buffer swap pipeline of the Croqtile tutorial
+// ch.6, section "使用 swap 的双缓冲": K is cut into tiles of 16
+// ("with tile_k in 16"); the prologue issues the asynchronous copy of tile 0
+// into buffer 0; each steady iteration t = 1..T-1 ("foreach tile_k(1:)")
+// issues tile t into the other buffer, multiplies the buffer holding tile
+// t-1, and swaps the two buffer names (a register swap; no data moves --
+// section "swap：交换的是名称，不是字节"); the epilogue multiplies the last
+// tile.  The copies are cp.async; as the TileLang tutorial ch.22 section 4.3
+// notes, __syncthreads does not wait for them, so every read of a buffer is
+// preceded by cp.async.wait_group and then __syncthreads (read after write),
+// and every refill by a __syncthreads after the last read (write after read).
+//
+// Each thread owns a TM x TN block of outputs held in registers and does
+// TM*TN wrapping 32-bit multiply-adds per K step (IMAD).
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "pwsgemm.h"
+
+namespace pws {
+namespace s32nn {
+
+constexpr int BK = 16;          // K per tile (the page's 256 / #tile_k)
+constexpr int THREADS = 256;
+constexpr int APAD = 4;         // words of padding per A row in shared memory
+
+template <int BM, int BN, int TM, int TN, int ABYTES, int BBYTES>
+__global__ void __launch_bounds__(THREADS)
+gemm_s32_nn_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, const int32_t* __restrict__ rhs,
+                   int32_t* __restrict__ out) {
+    static_assert((BM / TM) * (BN / TN) == THREADS, "one thread per TM x TN block");
+    // Two buffers per operand: A tiles [BM][BK] (k contiguous), B tiles [BK][BN].
+    __shared__ __align__(16) int32_t As[2][BM][BK + APAD];
+    __shared__ __align__(16) int32_t Bs[2][BK][BN];
+
+    const int tid = threadIdx.x;
+    const int tx = tid % (BN / TN);
+    const int ty = tid / (BN / TN);
+    const int m0 = blockIdx.y * BM;
+    const int n0 = blockIdx.x * BN;
+    const int T = (K + BK - 1) / BK;
+
+    // Issue the copies of K tile `t` into buffer `buf` (zero-fill outside M, N, K).
+    auto issue = [&](int t, int buf) {
+        const int k0 = t * BK;
+        constexpr int AE = ABYTES / 4;                 // int32 per A copy
+        constexpr int A_COPIES = BM * (BK / AE);
+        for (int i = tid; i < A_COPIES; i += THREADS) {
+            const int r = i / (BK / AE), c = (i % (BK / AE)) * AE;
+            const int gm = m0 + r, gk = k0 + c;
+            const bool ok = gm < M && gk < K;
+            const int32_t* src = ok ? lhs + (int64_t)gm * K + gk : lhs;
+            cp_async<ABYTES>(smem_u32(&As[buf][r][c]), src, ok ? ABYTES : 0);
+        }
+        constexpr int BE = BBYTES / 4;
+        constexpr int B_COPIES = BK * (BN / BE);
+        for (int i = tid; i < B_COPIES; i += THREADS) {
+            const int r = i / (BN / BE), c = (i % (BN / BE)) * BE;
+            const int gk = k0 + r, gn = n0 + c;
+            const bool ok = gk < K && gn < N;
+            const int32_t* src = ok ? rhs + (int64_t)gk * N + gn : rhs;
+            cp_async<BBYTES>(smem_u32(&Bs[buf][r][c]), src, ok ? BBYTES : 0);
+        }
+        cp_async_commit();
+    };
+
+    uint32_t acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0u;       // the zero start of "+="
+
+    // Multiply-accumulate over the 16 K values of buffer `buf`.
+    auto compute = [&](int buf) {
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            uint32_t a[TM], b[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) a[i] = static_cast<uint32_t>(As[buf][ty * TM + i][k]);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) b[j] = static_cast<uint32_t>(Bs[buf][k][tx * TN + j]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] += a[i] * b[j];   // wraps mod 2^32
+        }
+    };
+
+    if (T > 0) {
+        // prologue: tile 0 into buffer 0
+        int cur = 0, nxt = 1;
+        issue(0, cur);
+        // steady state: load tile t, compute tile t-1, swap
+        for (int t = 1; t < T; ++t) {
+            issue(t, nxt);
+            cp_async_wait_group<1>();      // tile t-1 has landed ...
+            __syncthreads();               // ... and is visible to every thread
+            compute(cur);
+            __syncthreads();               // everyone is done reading `cur` before it is refilled
+            const int tmp = cur;           // swap the names, not the bytes
+            cur = nxt;
+            nxt = tmp;
+        }
+        // epilogue: compute the last tile
+        cp_async_wait_group<0>();
+        __syncthreads();
+        compute(cur);
+    }
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int gm = m0 + ty * TM + i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int gn = n0 + tx * TN + j;
+            if (gn < N) out[(int64_t)gm * N + gn] = static_cast<int32_t>(acc[i][j]);
+        }
+    }
+}
+
+template <int BM, int BN, int TM, int TN>
+cudaError_t launch_tile(int M, int N, int K, const int32_t* lhs, const int32_t* rhs, int32_t* out,
+                        bool a16, bool b16, cudaStream_t stream) {
+    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+    // 16-byte copies need 16-byte aligned rows; otherwise one element per copy.
+    const bool b_vec = b16 && BN % 4 == 0;
+    if (a16 && b_vec)
+        gemm_s32_nn_kernel<BM, BN, TM, TN, 16, 16><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+    else if (a16)
+        gemm_s32_nn_kernel<BM, BN, TM, TN, 16, 4><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+    else if (b_vec)
+        gemm_s32_nn_kernel<BM, BN, TM, TN, 4, 16><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+    else
+        gemm_s32_nn_kernel<BM, BN, TM, TN, 4, 4><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+    return cudaGetLastError();
+}
+
+}  // namespace s32nn
+}  // namespace pws
+
+extern "C" int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32_t* rhs,
+                           int32_t* out, cudaStream_t stream) {
+    using namespace pws;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!out || (K > 0 && (!lhs || !rhs))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lhs) |
+         reinterpret_cast<uintptr_t>(rhs)) & 3u)
+        return GEMM_ERR_ALIGNMENT;
+    const uint64_t out_b = (uint64_t)M * N * 4;
+    if (K > 0 && (ranges_overlap(out, out_b, lhs, (uint64_t)M * K * 4) ||
+                  ranges_overlap(out, out_b, rhs, (uint64_t)K * N * 4)))
+        return GEMM_ERR_INVALID_ARG;
+
+    DeviceInfo info;
+    const int rc = current_device(&info);
+    if (rc != GEMM_OK) return rc;
+
+    const bool a16 = (K % 4 == 0) && (reinterpret_cast<uintptr_t>(lhs) % 16 == 0);
+    const bool b16 = (N % 4 == 0) && (reinterpret_cast<uintptr_t>(rhs) % 16 == 0);
+    // Largest output tile that still gives at least one block per SM; the
+    // smallest (16 x 16, one output per thread: the page's [16,16]-thread
+    // blocks) when none does.
+    auto blocks = [&](int bm, int bn) { return ((M + bm - 1) / bm) * ((N + bn - 1) / bn); };
+    cudaError_t e;
+    if (blocks(128, 128) >= info.num_sms)
+        e = s32nn::launch_tile<128, 128, 8, 8>((int)M, (int)N, (int)K, lhs, rhs, out, a16, b16, stream);
+    else if (blocks(64, 64) >= info.num_sms)
+        e = s32nn::launch_tile<64, 64, 4, 4>((int)M, (int)N, (int)K, lhs, rhs, out, a16, b16, stream);
+    else if (blocks(32, 32) >= info.num_sms)
+        e = s32nn::launch_tile<32, 32, 2, 2>((int)M, (int)N, (int)K, lhs, rhs, out, a16, b16, stream);
+    else
+        e = s32nn::launch_tile<16, 16, 1, 1>((int)M, (int)N, (int)K, lhs, rhs, out, a16, b16, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}

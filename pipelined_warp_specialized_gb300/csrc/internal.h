@@ -1,0 +1,52 @@
+// internal.h -- host-side helpers shared by the translation units of the
+// library (not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace pws {
+
+// Bits of the device status word.
+enum : unsigned {
+    kStatusTimeout = 1u,          // a bounded wait expired
+    kStatusRoleProducer = 1u << 8,
+    kStatusRoleMma = 1u << 9,
+    kStatusRoleEpilogue = 1u << 10,
+};
+
+struct DeviceInfo {
+    int device = -1;
+    int cc_major = 0, cc_minor = 0;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    unsigned* status = nullptr;   // device address of this device's status word
+};
+
+// Fills `info` for the current device.  Returns GEMM_OK,
+// GEMM_ERR_UNSUPPORTED_ARCH (not compute capability 10.3) or GEMM_ERR_LAUNCH.
+int current_device(DeviceInfo* info);
+
+uint64_t wait_timeout_ns();
+unsigned debug_flags();
+
+// SM count of the current device if one is present, else the GB300 count.
+int sm_count_or_default();
+
+// Encodes a 2-D tiled tensor map over a row-major matrix of 2-byte elements:
+// `inner` elements per row, `outer` rows, `row_bytes` between rows; a box of
+// box_inner x box_outer elements with the 128-byte swizzle; out-of-bounds
+// elements load as zero.  Returns false if the driver rejects it.
+bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// True if [a, a+an) and [b, b+bn) (bytes) intersect.
+inline bool ranges_overlap(const void* a, uint64_t an, const void* b, uint64_t bn) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    if (an == 0 || bn == 0) return false;
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+}  // namespace pws

@@ -1,0 +1,157 @@
+// runtime.cu -- host runtime of the library: the per-device status word,
+// device checks, wait limit and debug flags, tensor-map encoding, and the
+// status entry points of the C ABI.
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "pwsgemm.h"
+
+namespace pws {
+
+namespace {
+
+// One status word per device (a __device__ variable exists once in every
+// context that loads this module).  Kernels OR status bits into it.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ready[kMaxDevices] = {};
+
+std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<unsigned> g_flags{0};
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+EncodeTiledFn encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+}  // namespace
+
+int current_device(DeviceInfo* info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_info_ready[dev]) {
+            *info = g_info[dev];
+        } else {
+            DeviceInfo d;
+            d.device = dev;
+            if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                    cudaSuccess)
+                return GEMM_ERR_LAUNCH;
+            if (d.cc_major == 10 && d.cc_minor == 3) {
+                void* p = nullptr;
+                if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return GEMM_ERR_LAUNCH;
+                d.status = static_cast<unsigned*>(p);
+            }
+            g_info[dev] = d;
+            g_info_ready[dev] = true;
+            *info = d;
+        }
+    }
+    if (info->cc_major != 10 || info->cc_minor != 3) return GEMM_ERR_UNSUPPORTED_ARCH;
+    return GEMM_OK;
+}
+
+uint64_t wait_timeout_ns() {
+    const uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
+    return t ? t : kDefaultTimeoutNs;
+}
+
+unsigned debug_flags() { return g_flags.load(std::memory_order_relaxed); }
+
+int sm_count_or_default() {
+    int dev = -1, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+        return n;
+    cudaGetLastError();   // clear the "no device" error of a CPU-only host
+    return 152;
+}
+
+bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace pws
+
+extern "C" {
+
+int gemm_device_status(cudaStream_t stream) {
+    pws::DeviceInfo info;
+    const int rc = pws::current_device(&info);
+    if (rc != GEMM_OK) return rc;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, info.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_LAUNCH;
+    if (word) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(info.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return GEMM_ERR_LAUNCH;
+    }
+    return (word & pws::kStatusTimeout) ? GEMM_ERR_TIMEOUT : GEMM_OK;
+}
+
+const char* gemm_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+        case GEMM_ERR_UNSUPPORTED_STAGES: return "GEMM_ERR_UNSUPPORTED_STAGES";
+        case GEMM_ERR_UNSUPPORTED_ARCH: return "GEMM_ERR_UNSUPPORTED_ARCH";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+        default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+int gemm_set_wait_timeout_ns(uint64_t ns) {
+    pws::g_timeout_ns.store(ns, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+int gemm_set_debug_flags(unsigned flags) {
+    const unsigned known = GEMM_DEBUG_SKIP_EMPTY_SEED | GEMM_DEBUG_FORCE_COPY_PRODUCER |
+                           GEMM_DEBUG_FORCE_DIRECT_STORE | GEMM_DEBUG_FORCE_SOLO_TILE |
+                           GEMM_DEBUG_FORCE_PAIR_TILE;
+    if (flags & ~known) return GEMM_ERR_INVALID_ARG;
+    pws::g_flags.store(flags, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+"""The C-ABI library on the host (no GPU): it builds, loads, exports every
+function its header declares, and its host logic (argument checks, launch
+plan) behaves as the header states.  No call here launches a kernel."""
+import ctypes
+
+import pytest
+
+import pipelined_warp_specialized_gb300 as pws
+from pipelined_warp_specialized_gb300 import build as libbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return pws.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = pws.header_functions()
+    assert set(names) >= {"gemm_s32_nn", "gemm_f16_nt", "gemm_device_status", "gemm_status_string",
+                          "gemm_set_wait_timeout_ns", "gemm_set_debug_flags", "gemm_f16_nt_plan"}
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "GEMM_OK"), (1, "GEMM_ERR_INVALID_ARG"), (2, "GEMM_ERR_ALIGNMENT"),
+                       (3, "GEMM_ERR_UNSUPPORTED_STAGES"), (4, "GEMM_ERR_UNSUPPORTED_ARCH"),
+                       (5, "GEMM_ERR_LAUNCH"), (6, "GEMM_ERR_TIMEOUT")]:
+        assert pws.gemm_status_string(code) == name
+    assert pws.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+A = 1 << 40            # fake, 16-byte aligned addresses: never dereferenced on these paths
+B = 2 << 40
+C = 3 << 40
+
+
+@pytest.mark.parametrize("args,want", [
+    ((-1, 4, 4, A, B, C, 2), pws.GEMM_ERR_INVALID_ARG),
+    ((4, -1, 4, A, B, C, 2), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, -1, A, B, C, 2), pws.GEMM_ERR_INVALID_ARG),
+    ((1 << 31, 4, 4, A, B, C, 2), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, 4, A, B, C, 0), pws.GEMM_ERR_UNSUPPORTED_STAGES),
+    ((4, 4, 4, A, B, C, 7), pws.GEMM_ERR_UNSUPPORTED_STAGES),
+    ((4, 4, 4, 0, B, C, 2), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, 4, A, B, 0, 2), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, 4, A + 1, B, C, 2), pws.GEMM_ERR_ALIGNMENT),
+    ((4, 4, 4, A, B, A + 16, 2), pws.GEMM_ERR_INVALID_ARG),     # out overlaps lhs
+    ((0, 4, 4, 0, 0, 0, 2), pws.GEMM_OK),                       # empty output: no-op
+    ((4, 0, 4, 0, 0, 0, 6), pws.GEMM_OK),
+])
+def test_f16_argument_checks_return_before_launch(lib, args, want):
+    M, N, K, a, b, c, s = args
+    assert lib.gemm_f16_nt(M, N, K, a, b, c, s, None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((-1, 4, 4, A, B, C), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, 4, A, 0, C), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, 4, A + 2, B, C), pws.GEMM_ERR_ALIGNMENT),
+    ((4, 4, 4, A, B, B + 4), pws.GEMM_ERR_INVALID_ARG),          # out overlaps rhs
+    ((0, 4, 4, 0, 0, 0), pws.GEMM_OK),
+])
+def test_s32_argument_checks_return_before_launch(lib, args, want):
+    assert lib.gemm_s32_nn(*args, None) == want
+
+
+def test_debug_flags_and_timeout_setters(lib):
+    assert lib.gemm_set_debug_flags(1 << 10) == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_debug_flags(0) == pws.GEMM_OK
+    assert lib.gemm_set_wait_timeout_ns(0) == pws.GEMM_OK
+
+
+def test_plan_headline_shapes(lib):
+    pws.gemm_set_debug_flags(0)
+    p = pws.gemm_f16_nt_plan(8192, 8192, 8192, stages=6)
+    assert (p["bm"], p["bn"], p["bk"], p["cta_group"]) == (256, 256, 64, 2)
+    assert p["producer"] == 0 and p["store"] == 0
+    assert p["tiles"] == 32 * 32 and p["k_blocks"] == 128
+    # ring slots of 32 KB per CTA plus 32 KB of epilogue staging fit the 227 KB limit for every S
+    for s in range(1, 7):
+        q = pws.gemm_f16_nt_plan(8192, 8192, 8192, stages=s)
+        assert q["smem_bytes"] <= 232448
+        assert q["smem_bytes"] >= s * 32768 + 32768
+        assert {k: v for k, v in q.items() if k != "smem_bytes"} == {k: v for k, v in p.items() if k != "smem_bytes"}
+
+
+def test_plan_ragged_shape_uses_copy_producer(lib):
+    # K = 2050: rows of 4100 bytes are not 16-byte aligned, so no TMA descriptor exists
+    p = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
+    assert p["producer"] == 1 and p["copy_bytes"] == 4
+    assert p["cta_group"] == 1 and p["bm"] == 128
+    assert p["store"] == 0                      # 6000-byte output rows are 16-byte aligned
+    assert p["tiles"] == 32 * 24 and p["k_blocks"] == 33
+
+
+def test_plan_edge_cases(lib):
+    assert pws.gemm_f16_nt_plan(7, 9, 3)["copy_bytes"] == 2          # odd K: 2-byte copies
+    assert pws.gemm_f16_nt_plan(7, 9, 3)["store"] == 1               # odd N: plain stores
+    assert pws.gemm_f16_nt_plan(64, 64, 12)["copy_bytes"] == 8       # K % 4 == 0, not % 8
+    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 1   # unaligned base
+    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["copy_bytes"] == 2
+    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 8)["copy_bytes"] == 8
+    with pytest.raises(pws.GemmError):
+        pws.gemm_f16_nt_plan(64, 64, 16, stages=9)
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE)
+    try:
+        assert pws.gemm_f16_nt_plan(300, 300, 64)["cta_group"] == 2
+        assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 1   # copy producer: single CTA
+    finally:
+        pws.gemm_set_debug_flags(0)
+
+
+def test_binding_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(TypeError):
+        pws.gemm_f16_nt(torch.zeros(2, 2, dtype=torch.float32), torch.zeros(2, 2, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        pws.gemm_s32_nn(torch.zeros(2, 3, dtype=torch.int32), torch.zeros(2, 3, dtype=torch.int32))
+    with pytest.raises(ValueError):   # CPU tensors are refused, never computed on the host
+        pws.gemm_f16_nt(torch.zeros(2, 2, dtype=torch.float16), torch.zeros(2, 2, dtype=torch.float16))

@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA kernels, called through the C ABI, against the CPU oracle
+on the same seeded inputs.
+
+s32 is bit-exact.  f16 satisfies |gpu - ref| <= ulp16(ref) + 1e-3 sqrt(K)
+(ref = the float64 oracle), is bit-exact where the exact sum is a binary16
+value (closed forms), and is bitwise identical across stage counts S = 1..6.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import pipelined_warp_specialized_gb300 as pws
+from pipelined_warp_specialized_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from pipelined_warp_specialized_gb300 import build as libbuild
+    libbuild.build()
+    oracle.build()
+    pws.load_library()
+    pws.gemm_set_debug_flags(0)
+    yield torch.device("cuda:0")
+    pws.gemm_set_debug_flags(0)
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def run_f16(a, b, stages, flags=0):
+    pws.gemm_set_debug_flags(flags)
+    try:
+        out = pws.gemm_f16_nt(_dev(a), _dev(b), stages=stages)
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_OK
+    finally:
+        pws.gemm_set_debug_flags(0)
+    return out.cpu().numpy()
+
+
+def run_s32(a, b):
+    out = pws.gemm_s32_nn(_dev(a), _dev(b))
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def assert_f16_ok(gpu, ref, K):
+    res = oracle.check_f16(gpu, ref, K)
+    assert res["ok"], res
+
+
+# ------------------------------------------------------------------ s32 NN
+
+def test_s32_page_config_bit_exact():
+    wl = inputs.WORKLOADS["s32_nn_128x256x256"]
+    a, b = wl.lhs(), wl.rhs()
+    assert np.array_equal(run_s32(a, b), oracle.gemm_s32_nn(a, b))
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 1), (1, 300, 1), (17, 33, 15), (129, 257, 17), (64, 64, 16), (300, 500, 77),
+    (1000, 1000, 1000), (2048, 2048, 48), (5, 7, 3),
+])
+def test_s32_shapes_bit_exact(M, N, K):
+    a = inputs.ints(M + 3, 0, (M, K), -1000, 1000)
+    b = inputs.ints(N + 5, 1, (K, N), -1000, 1000)
+    assert np.array_equal(run_s32(a, b), oracle.gemm_s32_nn(a, b))
+
+
+def test_s32_wraps_on_overflow():
+    M, N, K = 40, 24, 64
+    a = inputs.ints(1, 0, (M, K), -2**31, 2**31 - 1)
+    b = inputs.ints(1, 1, (K, N), -2**31, 2**31 - 1)
+    assert np.array_equal(run_s32(a, b), oracle.gemm_s32_nn(a, b))
+
+
+def test_s32_k_zero_and_unaligned_rows():
+    a = np.zeros((5, 0), np.int32)
+    b = np.zeros((0, 6), np.int32)
+    assert np.array_equal(run_s32(a, b), np.zeros((5, 6), np.int32))
+    # a row-major view starting one element in: 4-byte aligned only (element copies)
+    big = _dev(inputs.ints(9, 0, (33 * 18 + 1,), -50, 50))
+    a_t = big[1:].view(33, 18)
+    b_np = inputs.ints(9, 1, (18, 21), -50, 50)
+    out = pws.gemm_s32_nn(a_t, _dev(b_np))
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), oracle.gemm_s32_nn(a_t.cpu().numpy(), b_np))
+
+
+# ------------------------------------------------------------------ f16 NT
+
+def test_f16_1024_config_full():
+    wl = inputs.WORKLOADS["f16_nt_1024"]
+    a, b = wl.lhs(), wl.rhs()
+    assert_f16_ok(run_f16(a, b, 2), oracle.gemm_f16_nt_f64(a, b), wl.K)
+
+
+@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER],
+                         ids=["solo_tma", "pair_tma", "solo_copy"])
+def test_f16_stage_counts_bitwise_identical(flags):
+    M, N, K = 700, 650, 1000          # several tiles, ragged M and N, a K tail of 40
+    a = inputs.uniform_f16(31, 0, (M, K))
+    b = inputs.uniform_f16(31, 1, (N, K))
+    outs = [run_f16(a, b, s, flags) for s in range(1, 7)]
+    for s in range(1, 6):
+        assert np.array_equal(outs[s].view(np.uint16), outs[0].view(np.uint16)), f"S={s + 1} differs from S=1"
+    assert_f16_ok(outs[0], oracle.gemm_f16_nt_f64(a, b), K)
+
+
+@pytest.mark.parametrize("M,N,K,flags", [
+    (1, 1, 1, 0), (1, 1, 8, 0), (5, 3, 64, 0), (128, 128, 64, 0), (129, 130, 72, 0),
+    (260, 300, 136, pws.GEMM_DEBUG_FORCE_PAIR_TILE),      # second pair row: the peer CTA is all padding
+    (513, 257, 200, pws.GEMM_DEBUG_FORCE_PAIR_TILE),
+    (65, 70, 33, 0),                                     # odd K: 2-byte element copies
+    (96, 80, 34, 0),                                     # K % 4 == 2: 4-byte copies
+    (96, 80, 44, 0),                                     # K % 8 == 4: 8-byte copies
+    (100, 77, 64, 0),                                    # odd N: guarded plain stores
+    (200, 136, 128, pws.GEMM_DEBUG_FORCE_DIRECT_STORE),
+    (300, 280, 512, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER | pws.GEMM_DEBUG_FORCE_DIRECT_STORE),
+])
+def test_f16_edge_shapes(M, N, K, flags):
+    a = inputs.normal_f16(M * 3 + K, 0, (M, K))
+    b = inputs.normal_f16(N * 7 + K, 1, (N, K))
+    for s in (1, 3):
+        assert_f16_ok(run_f16(a, b, s, flags), oracle.gemm_f16_nt_f64(a, b), K)
+
+
+def test_f16_k_zero_and_empty():
+    a = np.zeros((7, 0), np.float16)
+    b = np.zeros((5, 0), np.float16)
+    assert np.array_equal(run_f16(a, b, 2).view(np.uint16), np.zeros((7, 5), np.uint16))
+    out = pws.gemm_f16_nt(torch.zeros(0, 16, dtype=torch.float16, device="cuda"),
+                          torch.zeros(4, 16, dtype=torch.float16, device="cuda"))
+    assert out.shape == (0, 4)
+
+
+def test_f16_unaligned_operands():
+    M, N, K = 150, 90, 128
+    big_a = _dev(inputs.uniform_f16(5, 0, (M * K + 1,)))
+    a_t = big_a[1:].view(M, K)                           # 2-byte aligned only
+    b = inputs.uniform_f16(5, 1, (N, K))
+    out = pws.gemm_f16_nt(a_t, _dev(b), stages=2)
+    torch.cuda.synchronize()
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b), K)
+
+
+@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER])
+def test_f16_closed_forms_bit_exact(flags):
+    # rank one with dyadic values: every sum is K * a_m * b_n, exact in fp32 and in f16
+    K = 1024
+    a = np.array([1.0, -1.0, 0.5, -0.5] * 75, np.float16)            # M = 300
+    b = np.array([0.5, 1.0, -1.0, -0.5, 1.0] * 52, np.float16)       # N = 260
+    A = np.repeat(a[:, None], K, axis=1)
+    B = np.repeat(b[:, None], K, axis=1)
+    got = run_f16(A, B, 3, flags)
+    want = (K * np.outer(a.astype(np.float64), b.astype(np.float64))).astype(np.float16)
+    assert np.array_equal(got.view(np.uint16), want.view(np.uint16))
+    # identity: out = B^T exactly
+    Kp = 256
+    eye = np.eye(Kp, dtype=np.float16)
+    Bm = inputs.normal_f16(3, 1, (200, Kp))
+    got = run_f16(eye, Bm, 2, flags)
+    assert np.array_equal(got.view(np.uint16), np.ascontiguousarray(Bm.T).view(np.uint16))
+
+
+def test_f16_overflow_gives_inf():
+    A = np.full((130, 16), 256.0, np.float16)
+    B = np.full((140, 16), 256.0, np.float16)
+    B[1] = -256.0
+    got = run_f16(A, B, 2).astype(np.float64)
+    assert np.all(np.isposinf(got[:, 0])) and np.all(np.isneginf(got[:, 1]))
+
+
+def _sampled_entries(M, N, seed, n_random, tile=128):
+    rng = np.random.default_rng(seed)
+    rows = sorted({0, M - 1, tile - 1, tile, 2 * tile - 1, 2 * tile, M // 2} & set(range(M)))
+    cols = sorted({0, N - 1, tile - 1, tile, 2 * tile - 1, 2 * tile, N // 2} & set(range(N)))
+    rr, cc = [], []
+    for r in rows:                       # full rows crossing every column tile
+        rr.append(np.full(N, r))
+        cc.append(np.arange(N))
+    for c in cols:                       # full columns crossing every row tile
+        rr.append(np.arange(M))
+        cc.append(np.full(M, c))
+    rr.append(rng.integers(0, M, n_random))
+    cc.append(rng.integers(0, N, n_random))
+    return np.concatenate(rr), np.concatenate(cc)
+
+
+def test_f16_4096_config_sampled():
+    wl = inputs.WORKLOADS["f16_nt_4096"]
+    a, b = wl.lhs(), wl.rhs()
+    got = run_f16(a, b, 4)
+    rows, cols = _sampled_entries(wl.M, wl.N, 3, 50000)
+    ref = oracle.gemm_f16_nt_entries(a, b, rows, cols)
+    assert_f16_ok(got[rows, cols], ref, wl.K)
+
+
+def test_f16_ragged_config_full():
+    wl = inputs.WORKLOADS["f16_nt_ragged_4000x3000x2050"]
+    a, b = wl.lhs(), wl.rhs()
+    assert pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K)["producer"] == 1
+    assert_f16_ok(run_f16(a, b, 3), oracle.gemm_f16_nt_f64(a, b), wl.K)
+
+
+def test_f16_8192_sweep_identical_across_stages():
+    wl = inputs.WORKLOADS["f16_nt_8192"]
+    a, b = wl.lhs(), wl.rhs()
+    da, db = _dev(a), _dev(b)
+    first = None
+    for s in wl.stages:
+        out = pws.gemm_f16_nt(da, db, stages=s)
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_OK
+        if first is None:
+            first = out
+        else:
+            assert torch.equal(out.view(torch.int16), first.view(torch.int16)), f"S={s} differs"
+    rows, cols = _sampled_entries(wl.M, wl.N, 5, 20000, tile=256)
+    ref = oracle.gemm_f16_nt_entries(a, b, rows, cols)
+    assert_f16_ok(first.cpu().numpy()[rows, cols], ref, wl.K)
