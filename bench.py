@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the pipelined, warp-specialized GEMM library on GB300.
+
+One step = one f16 NT GEMM over the headline workload (default 8192^3,
+lhs [M,K] and rhs [N,K] f16 uniform in [-1,1] from seed 5, fp32 accumulate,
+f16 out), launched through the C ABI.  The inputs stay resident in HBM during
+the timed region and are larger than the 129 MB L2 (256 MB of operands), so
+no L2 flush is needed between steps.
+
+Prints ONE JSON line (rank 0):
+  value / ms_per_step   -- device time of K back-to-back steps (CUDA events on
+                           the launching stream, barrier + synchronize on both
+                           sides, max over ranks)
+  e2e                   -- the same metric through the C ABI with the inputs in
+                           pinned HOST memory: each step copies lhs and rhs to
+                           the device, runs the GEMM and copies out back
+  roofline              -- the GEMM kernel's achieved TFLOP/s against the
+                           measured dense 16-bit tensor peak
+  cpu_baseline          -- the CPU oracle timed on a bounded sample of the
+                           same workload on this host's cores
+  clocks                -- nvidia-smi samples taken during the timed region
+  configs               -- the other workloads (kernel-only timings): s32 NN
+                           128x256x256, f16 NT 1024^3 S=2, 4096^3 S=4, the
+                           ragged 4000x3000x2050 S=3 and the 8192^3 S=1..6 sweep
+
+--impl reference times the CPU oracle instead (the slow reference arm).
+With torchrun (N > 1) every rank runs an independent replica of the workload
+(weak scaling; the GEMM has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from pipelined_warp_specialized_gb300 import inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_f16_nt_8192_traffic.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "pipelined_warp_specialized_gb300", "csrc", "gemm_f16_nt.cu")
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(M, N, K):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this
+    shape, or None if absent or taken on another version of the kernel."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    vals = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    try:
+        if vals.get("kernel_sha") != kernel_sha():
+            return None
+        if (int(vals["M"]), int(vals["N"]), int(vals["K"])) != (M, N, K):
+            return None
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.interval}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)            # let the first sample land before timing starts
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [ln for ts, ln in self.lines if t0 - 0.06 <= ts <= t1 + 0.06] or [ln for _, ln in self.lines[-3:]]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in rows:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def time_launches(fn, steps, warmup, torch, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def extra_configs(pws, torch, stream, reps=20):
+    """Kernel-only timings of every workload (inputs resident)."""
+    out = {}
+    dev = torch.device("cuda")
+    wl = inputs.WORKLOADS["s32_nn_128x256x256"]
+    a = torch.from_numpy(wl.lhs()).to(dev)
+    b = torch.from_numpy(wl.rhs()).to(dev)
+    c = torch.empty(wl.M, wl.N, dtype=torch.int32, device=dev)
+    ms = time_launches(lambda: pws.gemm_s32_nn(a, b, c, stream=stream), 200, 20, torch, stream)
+    out[wl.name] = {"us": round(ms * 1e3, 2), "TOPS": round(wl.flops / ms / 1e9, 3),
+                    "GB_s": round((wl.M * wl.K + wl.K * wl.N + wl.M * wl.N) * 4 / ms / 1e6, 1)}
+    for name in ("f16_nt_1024", "f16_nt_4096", "f16_nt_ragged_4000x3000x2050", "f16_nt_8192"):
+        wl = inputs.WORKLOADS[name]
+        a = torch.from_numpy(wl.lhs()).to(dev)
+        b = torch.from_numpy(wl.rhs()).to(dev)
+        c = torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev)
+        plan = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), wl.stages[0])
+        res = {"producer": "tma" if plan["producer"] == 0 else f"cp.async{plan['copy_bytes']}B",
+               "cta_group": plan["cta_group"]}
+        n = reps if wl.M * wl.N * wl.K < 2 ** 36 else max(5, reps // 2)
+        for s in wl.stages:
+            ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3, torch, stream)
+            res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1)}
+        out[name] = res
+        del a, b, c
+    return out
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import pipelined_warp_specialized_gb300 as pws
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pws.load_library()
+    stream = torch.cuda.current_stream(dev)
+    M, N, K, S = args.M, args.N, args.K, args.stages
+    flops = 2.0 * M * N * K
+    # the seeded synthetic workload: uniform [-1, 1) rounded to f16, seed 5
+    a_h = torch.from_numpy(inputs.uniform_f16(5, 0, (M, K))).pin_memory()
+    b_h = torch.from_numpy(inputs.uniform_f16(5, 1, (N, K))).pin_memory()
+    c_h = torch.empty(M, N, dtype=torch.float16).pin_memory()
+    a = a_h.to(dev)
+    b = b_h.to(dev)
+    c = torch.empty(M, N, dtype=torch.float16, device=dev)
+
+    def step():
+        pws.gemm_f16_nt(a, b, c, stages=S, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = pws.gemm_device_status()
+    if status != pws.GEMM_OK:
+        raise RuntimeError(f"device status after warm-up: {pws.gemm_status_string(status)}")
+
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    status = pws.gemm_device_status()
+    if status != pws.GEMM_OK:
+        raise RuntimeError(f"device status after timing: {pws.gemm_status_string(status)}")
+    ms = ms_total / args.steps
+    value = world * flops / ms / 1e9          # TFLOP/s over all ranks
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        def e2e_step():
+            a.copy_(a_h, non_blocking=True)
+            b.copy_(b_h, non_blocking=True)
+            pws.gemm_f16_nt(a, b, c, stages=S, stream=stream)
+            c_h.copy_(c, non_blocking=True)
+        n_e2e = max(3, min(args.steps, 20))
+        ms_e2e = time_launches(e2e_step, n_e2e, 2, torch, stream)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": round(world * flops / ms_e2e / 1e9, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int((M * K + N * K) * 2), "d2h_bytes_per_step": int(M * N * 2),
+               "ms_per_step": round(ms_e2e, 4), "steps": n_e2e}
+
+    peaks, peak_src = measured_peaks()
+    long_region = ms_total > 1000.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    achieved = flops / ms / 1e9
+    roofline = {"bound": "tensor", "kernel": "gemm_f16_nt_kernel<2,S>" if M * N >= 2 ** 20 else "gemm_f16_nt_kernel",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_src} {'sustained' if long_region else 'burst'} dense bf16 "
+                               "(f16 and bf16 share the tensor rate)",
+                "traffic": profiled_traffic(M, N, K),
+                "algorithmic_bytes_per_launch": int((M * K + N * K + M * N) * 2)}
+
+    extras = None
+    if rank == 0 and world == 1 and not args.no_sweep and (M, N, K) == (8192, 8192, 8192):
+        extras = extra_configs(pws, torch, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        del a, b, c
+        cpu = cpu_baseline(M, N, K, args.cpu_seconds, a_h.numpy(), b_h.numpy())
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    line = {
+        "metric": "f16 NT GEMM TFLOP/s at 8192^3 (fraction of GB300 dense f16 tensor peak in roofline)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"f16_nt_{M}x{N}x{K}", "M": M, "N": N, "K": K, "stages": S,
+                   "accumulate": "f32", "layout": "lhs[M,K] rhs[N,K] out[M,N] row-major",
+                   "values": "uniform[-1,1) rounded to f16", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "gpu_launches": args.steps,
+        "roofline": roofline, "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu, "configs": extras,
+    }
+    return line
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_time(a, b, rows):
+    """Times the oracle on the first `rows` rows of lhs against all of rhs."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt_f64(a[:rows], b)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(M, N, K, seconds, a, b):
+    """The oracle as it stands on this host's cores, on a bounded sample of
+    the workload (the first rows of the output, all columns, full K)."""
+    import oracle
+    threads = oracle.default_threads()
+    probe_rows = max(1, threads)
+    t = oracle_time(a, b, probe_rows)
+    rows = int(max(1, min(M, probe_rows * max(1.0, seconds / max(t, 1e-3)))))
+    t = oracle_time(a, b, rows)
+    flops = 2.0 * rows * N * K
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {M} output rows x {N} columns, K={K} (f64 triple loop), {t:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on this host's cores."""
+    if rank != 0:
+        return None
+    import oracle
+    M, N, K = args.M, args.N, args.K
+    threads = oracle.default_threads()
+    b = inputs.uniform_f16(5, 1, (N, K))
+    a_probe = inputs.uniform_f16(5, 0, (max(1, threads), K))
+    # size one step so the whole warm-up + timed run stays within ~90 s
+    t = oracle_time(a_probe, b, max(1, threads))
+    per_row = t / max(1, threads)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(M, budget / max(per_row, 1e-6))))
+    a = inputs.uniform_f16(5, 0, (rows, K))
+    for _ in range(args.warmup):
+        oracle.gemm_f16_nt_f64(a, b)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_f16_nt_f64(a, b)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * N * K / dt / 1e12
+    sample = f"{rows} of {M} output rows x {N} columns, K={K} per step (f64 triple loop)"
+    return {
+        "impl": "reference", "metric": "f16 NT GEMM TFLOP/s at 8192^3 (fraction of GB300 dense f16 tensor peak in roofline)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"f16_nt_{M}x{N}x{K}", "M": M, "N": N, "K": K, "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--stages", type=int, default=6)
+    ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K of the timed GEMM")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload timings")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.M, args.N, args.K = (int(x) for x in args.shape.split(","))
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,54 @@
+"""The bounded device waits: skipping the empty-credit seed (the deadlock the
+Croqtile tutorial ch.6 describes in "消费者路径") must end in GEMM_ERR_TIMEOUT
+from the status word, with the kernel returning on its own and the context
+still usable.  Nothing here faults, traps or hangs the GPU: every wait in the
+kernels gives up after the limit set below, and the roles drain and return."""
+import numpy as np
+import pytest
+
+import oracle
+import pipelined_warp_specialized_gb300 as pws
+from pipelined_warp_specialized_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from pipelined_warp_specialized_gb300 import build as libbuild
+    libbuild.build()
+    pws.load_library()
+    yield
+    pws.gemm_set_debug_flags(0)
+    pws.gemm_set_wait_timeout_ns(0)
+
+
+@pytest.mark.parametrize("extra", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER],
+                         ids=["solo_tma", "pair_tma", "solo_copy"])
+def test_missing_seed_times_out_and_context_survives(extra):
+    M, N, K = 256, 256, 256
+    a_np = inputs.uniform_f16(2, 0, (M, K))
+    b_np = inputs.uniform_f16(2, 1, (N, K))
+    a = torch.from_numpy(a_np).cuda()
+    b = torch.from_numpy(b_np).cuda()
+    assert pws.gemm_device_status() == pws.GEMM_OK          # clear anything earlier
+    pws.gemm_set_wait_timeout_ns(200_000_000)               # 0.2 s per wait
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_SKIP_EMPTY_SEED | extra)
+    try:
+        pws.gemm_f16_nt(a, b, stages=2)
+        torch.cuda.synchronize()                             # the kernel returns by itself
+        assert pws.gemm_device_status() == pws.GEMM_ERR_TIMEOUT
+        assert pws.gemm_device_status() == pws.GEMM_OK       # the word was cleared
+    finally:
+        pws.gemm_set_debug_flags(0)
+        pws.gemm_set_wait_timeout_ns(0)
+    # the context is intact: a normal call still gives the right answer
+    out = pws.gemm_f16_nt(a, b, stages=2)
+    torch.cuda.synchronize()
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    res = oracle.check_f16(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_np, b_np), K)
+    assert res["ok"], res
+    assert np.isfinite(out.float().cpu().numpy()).all()
