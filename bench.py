@@ -61,6 +61,17 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The maximum of x over all ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -171,6 +182,59 @@ def time_launches(fn, steps, warmup, torch, stream):
     return e0.elapsed_time(e1) / steps
 
 
+def e2e_pipelined(pws, torch, dev, a_h, b_h, c_h, stages, n_steps, warmup=2):
+    """Average ms per step of host -> device -> GEMM -> host, pipelined over steps.
+
+    Every step copies its lhs and rhs from pinned host memory, runs the GEMM
+    through the C ABI and copies the result back to pinned host memory.  The
+    three phases run on three streams with two device buffers per operand;
+    events order each buffer's reuse (copy-in of step i+2 waits for the GEMM of
+    step i; the GEMM of step i+2 waits for the copy-out of step i).
+    """
+    M, K = a_h.shape
+    N = b_h.shape[0]
+    s_in, s_mm, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    a = [torch.empty(M, K, dtype=torch.float16, device=dev) for _ in range(2)]
+    b = [torch.empty(N, K, dtype=torch.float16, device=dev) for _ in range(2)]
+    c = [torch.empty(M, N, dtype=torch.float16, device=dev) for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_mm = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def step(i):
+        j = i % 2
+        with torch.cuda.stream(s_in):
+            if used[j]:
+                s_in.wait_event(ev_mm[j])          # the GEMM two steps back has read a[j], b[j]
+            a[j].copy_(a_h, non_blocking=True)
+            b[j].copy_(b_h, non_blocking=True)
+            ev_in[j].record(s_in)
+        s_mm.wait_event(ev_in[j])
+        if used[j]:
+            s_mm.wait_event(ev_out[j])             # the copy-out two steps back has read c[j]
+        pws.gemm_f16_nt(a[j], b[j], c[j], stages=stages, stream=s_mm)
+        ev_mm[j].record(s_mm)
+        s_out.wait_event(ev_mm[j])
+        with torch.cuda.stream(s_out):
+            c_h.copy_(c[j], non_blocking=True)
+            ev_out[j].record(s_out)
+        used[j] = True
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(n_steps):
+        step(warmup + i)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n_steps
+
+
 def extra_configs(pws, torch, stream, reps=20):
     """Kernel-only timings of every workload (inputs resident)."""
     out = {}
@@ -193,7 +257,8 @@ def extra_configs(pws, torch, stream, reps=20):
         n = reps if wl.M * wl.N * wl.K < 2 ** 36 else max(5, reps // 2)
         for s in wl.stages:
             ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3, torch, stream)
-            res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1)}
+            res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
+                            "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1)}
         out[name] = res
         del a, b, c
     return out
@@ -212,8 +277,8 @@ def run_ours(args, world, rank, local):
     M, N, K, S = args.M, args.N, args.K, args.stages
     flops = 2.0 * M * N * K
     # the seeded synthetic workload: uniform [-1, 1) rounded to f16, seed 5
-    a_h = torch.from_numpy(inputs.uniform_f16(5, 0, (M, K))).pin_memory()
-    b_h = torch.from_numpy(inputs.uniform_f16(5, 1, (N, K))).pin_memory()
+    a_h = torch.from_numpy(args.wl.lhs()).pin_memory()
+    b_h = torch.from_numpy(args.wl.rhs()).pin_memory()
     c_h = torch.empty(M, N, dtype=torch.float16).pin_memory()
     a = a_h.to(dev)
     b = b_h.to(dev)
@@ -249,10 +314,7 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     ms_total = e0.elapsed_time(e1)
     clocks = sampler.stop(t0, t1) if sampler else None
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     status = pws.gemm_device_status()
     if status != pws.GEMM_OK:
         raise RuntimeError(f"device status after timing: {pws.gemm_status_string(status)}")
@@ -262,20 +324,14 @@ def run_ours(args, world, rank, local):
     # end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        def e2e_step():
-            a.copy_(a_h, non_blocking=True)
-            b.copy_(b_h, non_blocking=True)
-            pws.gemm_f16_nt(a, b, c, stages=S, stream=stream)
-            c_h.copy_(c, non_blocking=True)
-        n_e2e = max(3, min(args.steps, 20))
-        ms_e2e = time_launches(e2e_step, n_e2e, 2, torch, stream)
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
+        n_e2e = max(3, min(args.steps, 30))
+        ms_e2e = max_over_ranks(e2e_pipelined(pws, torch, dev, a_h, b_h, c_h, S, n_e2e), world, dev)
         e2e = {"value": round(world * flops / ms_e2e / 1e9, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int((M * K + N * K) * 2), "d2h_bytes_per_step": int(M * N * 2),
-               "ms_per_step": round(ms_e2e, 4), "steps": n_e2e}
+               "ms_per_step": round(ms_e2e, 4), "steps": n_e2e,
+               "how": "pinned host lhs/rhs -> device, gemm_f16_nt, out -> pinned host, every step; "
+                      "copy-in, GEMM and copy-out run on three streams with double-buffered device "
+                      "operands, so step i's GEMM overlaps step i+1's copy-in and step i-1's copy-out"}
 
     peaks, peak_src = measured_peaks()
     long_region = ms_total > 1000.0
@@ -307,9 +363,10 @@ def run_ours(args, world, rank, local):
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"f16_nt_{M}x{N}x{K}", "M": M, "N": N, "K": K, "stages": S,
+        "config": {"workload": args.wl.name, "M": M, "N": N, "K": K, "stages": S,
                    "accumulate": "f32", "layout": "lhs[M,K] rhs[N,K] out[M,N] row-major",
-                   "values": "uniform[-1,1) rounded to f16", "parallelism": f"replicas x{world}",
+                   "values": f"{args.wl.dist} (seed {args.wl.seed}) rounded to f16",
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush)"},
         "gpu_launches": args.steps,
         "roofline": roofline, "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu, "configs": extras,
@@ -383,14 +440,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--stages", type=int, default=6)
-    ap.add_argument("--shape", default="8192,8192,8192", help="M,N,K of the timed GEMM")
+    ap.add_argument("--workload", default="f16_nt_8192", choices=[k for k in inputs.WORKLOADS if k.startswith("f16")],
+                    help="the seeded f16 workload of the timed GEMM")
+    ap.add_argument("--shape", default=None, help="M,N,K override (uniform [-1,1) inputs, seed 5)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload timings")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
-    args.M, args.N, args.K = (int(x) for x in args.shape.split(","))
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.split(","))
+        args.wl = inputs.Workload(f"f16_nt_{M}x{N}x{K}", "f16_nt", M, N, K, 5, "uniform", (args.stages,))
+    else:
+        args.wl = inputs.WORKLOADS[args.workload]
+    args.M, args.N, args.K = args.wl.M, args.wl.N, args.wl.K
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     world, rank, local = dist_env()

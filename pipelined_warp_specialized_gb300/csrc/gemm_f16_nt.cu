@@ -16,10 +16,11 @@
 //   * producer  -- one warp (one elected thread) issues the TMA copies:
 //                  wait empty[s], arm full[s] with the byte count, copy A and
 //                  B strips into slot s.  Where TMA cannot address the
-//                  operands (rows not 16-byte aligned), four warps fill the
+//                  operands (rows not 16-byte aligned), eight warps fill the
 //                  same swizzled layout with cp.async and arrive on full[s]
 //                  once their copies have landed and been fenced to the async
-//                  proxy (CUDA tutorial ch.4, section 4.8.1).
+//                  proxy (CUDA tutorial ch.4, section 4.8.1), S - 1 slots late
+//                  so that S - 1 slots of copies stay in flight.
 //   * consumer  -- one warp (one elected thread) seeds every empty[s] once
 //                  before its loop ("foreach {s} in [MATMUL_STAGES] trigger
 //                  empty[s]"), then per K block waits full[s], issues four
@@ -74,7 +75,8 @@ constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128
 constexpr int EPI_BUF = 32 * EPI_COLS * 2;     // 32 rows x 64 columns
 constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
 constexpr int MAX_STAGES = 6;
-constexpr int COPY_WARPS = 4;          // producer warps of the cp.async producer
+constexpr int COPY_WARPS = 8;          // producer warps of the cp.async producer
+constexpr int COPY_THREADS = COPY_WARPS * 32;
 constexpr int GROUP_M = 8;             // tile-row group height of the raster order
 
 enum { kProducerTma = 0, kProducerCopy = 1 };
@@ -193,6 +195,104 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// ---------------------------------------------------------------- copy producer
+//
+// Fills ring slots with cp.async where no tensor map can describe the
+// operands (rows not a multiple of 16 bytes, or an unaligned base).  The
+// slot layout is exactly the one TMA writes: row r of the strip at r * 128
+// bytes, 16-byte chunk c of the row at chunk (c ^ (r mod 8)).  Copies are G
+// bytes (8 or 4 with cp.async and zero fill; 2 with plain loads and stores).
+template <int G>
+struct CopyShape {
+    static constexpr int E = G / 2;                      // f16 per copy
+    static constexpr int CPR = 128 / G;                  // copies per 128-byte row
+    static constexpr int RPJ = COPY_THREADS / CPR;       // rows covered by one sweep of the threads
+    static constexpr int J = BM_CTA / RPJ;               // sweeps per 128-row strip
+    static_assert(COPY_THREADS % CPR == 0 && BM_CTA % RPJ == 0, "copy mapping");
+};
+
+// One 64-wide K strip of 128 rows of one operand into the slot at `slot`.
+// Thread t copies column (t mod CPR) of rows t / CPR + j * RPJ.
+template <int G>
+__device__ __forceinline__ void copy_strip(uint32_t slot, const __half* base, int rows_total, int row0, int K,
+                                           int k0, int t) {
+    using C = CopyShape<G>;
+    const int col = t % C::CPR;
+    const int rr0 = t / C::CPR;
+    const int k = k0 + col * C::E;
+    const uint32_t in_row = static_cast<uint32_t>(col * G);
+    const bool kval = k < K;
+    const int64_t row_step = static_cast<int64_t>(C::RPJ) * K;
+    const __half* src0 = base + static_cast<int64_t>(row0 + rr0) * K + k;
+    if constexpr (G == 2) {
+        unsigned short v[C::J];
+#pragma unroll
+        for (int j = 0; j < C::J; ++j) {
+            const bool ok = kval && row0 + rr0 + j * C::RPJ < rows_total;
+            v[j] = ok ? __ldg(reinterpret_cast<const unsigned short*>(src0 + j * row_step)) : (unsigned short)0;
+        }
+#pragma unroll
+        for (int j = 0; j < C::J; ++j) {
+            const int rr = rr0 + j * C::RPJ;
+            const uint32_t dst = slot + rr * 128 + (((in_row >> 4) ^ static_cast<uint32_t>(rr & 7)) << 4) + (in_row & 15u);
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst), "h"(v[j]) : "memory");
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < C::J; ++j) {
+            const int rr = rr0 + j * C::RPJ;
+            const bool ok = kval && row0 + rr < rows_total;
+            const __half* src = ok ? src0 + j * row_step : base;
+            const uint32_t dst = slot + rr * 128 + (((in_row >> 4) ^ static_cast<uint32_t>(rr & 7)) << 4) + (in_row & 15u);
+            cp_async<G>(dst, src, ok ? static_cast<uint32_t>(G) : 0u);
+        }
+    }
+}
+
+// The producer loop of the copy path.  Each thread's copies of K block k form
+// one cp.async group; the slot of block k is signalled LAG = S - 1 blocks
+// later, once the thread's groups up to k have landed (cp.async.wait_group),
+// after a proxy fence (the tensor core reads through the async proxy) and a
+// warp barrier, by one arrive per warp.  LAG <= S - 1 keeps the ring live:
+// the wait on empty for block k needs full for block k - S already signalled.
+template <int G, int S>
+__device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB, uint32_t bFULL,
+                              uint32_t bEMPTY, int cluster_id, int num_clusters, int lane) {
+    constexpr int LAG = S - 1;
+    const int t = threadIdx.x;                   // 0 .. COPY_THREADS - 1
+    uint32_t stage = 0, phase = 0, issued = 0, signalled = 0;
+    bool ok = true;
+    for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+        int tm, tn;
+        tile_coords(tile, p, tm, tn);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            bool got = true;
+            if (lane == 0) got = W.wait(bEMPTY + 8 * stage, phase);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) { ok = false; break; }
+            copy_strip<G>(sA + stage * A_SLOT, p.lhs, p.M, tm * BM_CTA, p.K, kb * BK, t);
+            copy_strip<G>(sB + stage * B_SLOT, p.rhs, p.N, tn * BN_CTA, p.K, kb * BK, t);
+            cp_async_commit();
+            ++issued;
+            if (issued - signalled > static_cast<uint32_t>(LAG)) {
+                cp_async_wait_group<LAG>();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bFULL + 8 * (signalled % S));
+                ++signalled;
+            }
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+    }
+    cp_async_wait_group<0>();
+    if (ok) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        for (; signalled < issued; ++signalled)
+            if (lane == 0) mbar_arrive(bFULL + 8 * (signalled % S));
+    }
+}
+
 template <int CG, int S>
 __global__ void __launch_bounds__((COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -221,7 +321,8 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
-        const uint32_t full_count = p.producer == kProducerTma ? 1u : static_cast<uint32_t>(P * 32);
+        // TMA: one arrive.expect_tx per phase; cp.async: one arrive per producer warp
+        const uint32_t full_count = p.producer == kProducerTma ? 1u : static_cast<uint32_t>(P);
         for (int s = 0; s < S; ++s) {
             mbar_init(bFULL + 8 * s, full_count);
             mbar_init(bEMPTY + 8 * s, 1);
@@ -294,74 +395,14 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 }
             }
         } else if constexpr (CG == 1) {
-            // cp.async producer (single CTA only): P warps fill the swizzled slot
+            // cp.async producer (single CTA only): COPY_WARPS warps fill the swizzled slot
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
-            const int ptid = threadIdx.x;                 // 0 .. P*32-1
-            const int nthr = P * 32;
-            const int G = p.copy_bytes;                  // bytes per copy
-            const int E = G / 2;                         // f16 per copy
-            const int per_row = BK / E;
-            uint32_t stage = 0, phase = 0;
-            int prev = -1;
-            bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-                int tm, tn;
-                tile_coords(t, p, tm, tn);
-                const int m_cta = tm * SH::UMMA_M;
-                const int n_cta = tn * SH::UMMA_N;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    bool got = true;
-                    if (lane == 0) got = W.wait(bEMPTY + 8 * stage, phase);
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) { ok = false; break; }
-                    const int k0 = kb * BK;
-                    for (int op = 0; op < 2; ++op) {
-                        const __half* src_base = op == 0 ? p.lhs : p.rhs;
-                        const int rows_total = op == 0 ? p.M : p.N;
-                        const int row0 = op == 0 ? m_cta : n_cta;
-                        const uint32_t dst_base = (op == 0 ? sA + stage * A_SLOT : sB + stage * B_SLOT);
-                        for (int i = ptid; i < BM_CTA * per_row; i += nthr) {
-                            const int r = i / per_row;
-                            const int c = (i - r * per_row) * E;        // f16 column inside the strip
-                            const int gr = row0 + r, gk = k0 + c;
-                            const bool valid = gr < rows_total && gk < p.K;
-                            const uint32_t bo = static_cast<uint32_t>(c * 2);
-                            const uint32_t dst = dst_base + r * 128 +
-                                                 ((((bo >> 4) ^ static_cast<uint32_t>(r & 7)) << 4) | (bo & 15u));
-                            const __half* src = valid ? src_base + static_cast<int64_t>(gr) * p.K + gk : src_base;
-                            if (G == 8) {
-                                cp_async<8>(dst, src, valid ? 8u : 0u);
-                            } else if (G == 4) {
-                                cp_async<4>(dst, src, valid ? 4u : 0u);
-                            } else {
-                                const unsigned short v =
-                                    valid ? __ldg(reinterpret_cast<const unsigned short*>(src)) : (unsigned short)0;
-                                asm volatile("st.shared.u16 [%0], %1;" ::"r"(dst), "h"(v) : "memory");
-                            }
-                        }
-                    }
-                    cp_async_commit();
-                    if (S > 1) {
-                        // signal the previous slot once its copies have landed
-                        if (prev >= 0) {
-                            cp_async_wait_group<1>();
-                            fence_proxy_async_smem();
-                            mbar_arrive(bFULL + 8 * prev);
-                        }
-                        prev = static_cast<int>(stage);
-                    } else {
-                        cp_async_wait_group<0>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(bFULL + 8 * stage);
-                    }
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                }
-            }
-            cp_async_wait_group<0>();
-            if (ok && S > 1 && prev >= 0) {
-                fence_proxy_async_smem();
-                mbar_arrive(bFULL + 8 * prev);
-            }
+            if (p.copy_bytes == 8)
+                copy_producer<8, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, lane);
+            else if (p.copy_bytes == 4)
+                copy_producer<4, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, lane);
+            else
+                copy_producer<2, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, lane);
         }
         __syncwarp();
     } else if (warp == mma_warp) {
