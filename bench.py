@@ -251,15 +251,26 @@ def extra_configs(pws, torch, stream, reps=20):
         a = torch.from_numpy(wl.lhs()).to(dev)
         b = torch.from_numpy(wl.rhs()).to(dev)
         c = torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev)
-        plan = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), wl.stages[0])
-        res = {"producer": "tma" if plan["producer"] == 0 else f"cp.async{plan['copy_bytes']}B",
-               "cta_group": plan["cta_group"]}
-        n = reps if wl.M * wl.N * wl.K < 2 ** 36 else max(5, reps // 2)
-        for s in wl.stages:
-            ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3, torch, stream)
-            res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
-                            "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1)}
-        out[name] = res
+        # the ragged shape is timed on both of its paths: repack + TMA (the
+        # default) and the async-copy producer reading the operands in place
+        variants = [("", 0)]
+        if name.startswith("f16_nt_ragged"):
+            variants.append(("copy_producer", pws.GEMM_DEBUG_FORCE_COPY_PRODUCER))
+        for suffix, flags in variants:
+            pws.gemm_set_debug_flags(flags)
+            try:
+                plan = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), wl.stages[0])
+                label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B", 2: "repack+tma"}[plan["producer"]]
+                res = {"producer": label, "cta_group": plan["cta_group"]}
+                n = reps if wl.M * wl.N * wl.K < 2 ** 36 else max(5, reps // 2)
+                for s in wl.stages:
+                    ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3,
+                                       torch, stream)
+                    res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
+                                    "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1)}
+            finally:
+                pws.gemm_set_debug_flags(0)
+            out[name + ("/" + suffix if suffix else "")] = res
         del a, b, c
     return out
 

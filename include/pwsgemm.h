@@ -95,10 +95,17 @@ int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32
  *            single-buffer case (load and multiply serialise).  The result is
  *            bitwise identical for every S.
  *
- * The producer uses the tensor memory accelerator when both operands start
- * on 16-byte boundaries and K is a multiple of 8 (row stride a multiple of 16
- * bytes); otherwise an asynchronous-copy producer fills the same swizzled
- * ring.  Partial tiles are zero-filled on load and clipped on store.
+ * The producer uses the tensor memory accelerator (TMA) when both operands
+ * start on 16-byte boundaries and K is a multiple of 8 (row stride a multiple
+ * of 16 bytes).  Otherwise the call first copies both operands into rows of
+ * ceil(K/8)*8 elements in scratch memory taken, stream-ordered, from a memory
+ * pool the library owns on the current device ((M+N)*ceil(K/8)*16 bytes,
+ * returned to the pool on `stream` after the GEMM; the pool keeps freed
+ * memory for the next call, so repeated calls of one size request no new
+ * memory and never synchronize).  If the pool cannot supply it, an
+ * asynchronous-copy producer fills the same swizzled ring straight from the
+ * operands instead.  Partial tiles are zero-filled on load and clipped on
+ * store.
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT (a pointer not
  * 2-byte aligned), GEMM_ERR_UNSUPPORTED_STAGES, GEMM_ERR_UNSUPPORTED_ARCH or
@@ -162,7 +169,8 @@ int gemm_set_debug_flags(unsigned flags);
  * arguments exactly as gemm_f16_nt does and returns the same status.
  *   plan[0] tile rows per CTA group (BM)      plan[1] tile columns (BN)
  *   plan[2] K per ring slot (BK)              plan[3] CTAs per tile (1 or 2)
- *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy
+ *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy,
+ *           2 = tensor memory accelerator on a 16-byte aligned scratch copy
  *   plan[5] copy granularity in bytes (16 for TMA, else 8, 4 or 2)
  *   plan[6] output store: 0 = tensor memory accelerator, 1 = plain stores
  *   plan[7] dynamic shared memory bytes per CTA

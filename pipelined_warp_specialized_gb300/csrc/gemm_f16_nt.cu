@@ -51,6 +51,7 @@
 // the other roles poll, and every role then runs the common exit path, so
 // the kernel always returns.
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 
 #include <cuda.h>
@@ -555,8 +556,52 @@ __global__ void zero_fill_u16(unsigned short* out, int64_t n) {
         out[i] = 0;
 }
 
+// Copies the rows of lhs [ma, K] and rhs [nb, K] into rows of Kp = K rounded
+// up to 8 elements (16 bytes), the padding zeroed: a layout the tensor memory
+// accelerator can address when K * 2 bytes is not a multiple of 16 or a base
+// is not 16-byte aligned.  One thread writes one 16-byte chunk of a
+// destination row; `pairs` means 4-byte source loads are aligned (K even and
+// both bases 4-byte aligned).
+__global__ void __launch_bounds__(256)
+repack_rows_kernel(const uint16_t* __restrict__ a, int64_t ma, const uint16_t* __restrict__ b, int64_t nb, int K,
+                   int Kp, uint16_t* __restrict__ dst_a, uint16_t* __restrict__ dst_b, int pairs) {
+    const int64_t chunks = Kp / 8;
+    const int64_t total = (ma + nb) * chunks;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int64_t r = i / chunks;
+        const int k0 = static_cast<int>(i - r * chunks) * 8;
+        const uint16_t* src;
+        uint16_t* dst;
+        if (r < ma) {
+            src = a + r * K;
+            dst = dst_a + r * Kp;
+        } else {
+            r -= ma;
+            src = b + r * K;
+            dst = dst_b + r * Kp;
+        }
+        uint32_t w[4];
+        if (pairs && k0 + 8 <= K) {
+            const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src + k0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[j] = __ldg(s4 + j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = k0 + 2 * j;
+                const uint32_t lo = k < K ? __ldg(src + k) : 0u;
+                const uint32_t hi = k + 1 < K ? __ldg(src + k + 1) : 0u;
+                w[j] = lo | (hi << 16);
+            }
+        }
+        *reinterpret_cast<uint4*>(dst + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 struct Plan {
     int cg = 1;
+    bool repack = false;        // operands copied to 16-byte aligned rows, then TMA
     int producer = kProducerTma;
     int copy_bytes = 16;
     int store = kStoreTma;
@@ -594,13 +639,27 @@ int validate(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, 
     return GEMM_OK;
 }
 
+// Bytes of scratch the repack path needs: both operands with rows of Kp.
+inline size_t repack_bytes(int64_t M, int64_t N, int64_t K, size_t* b_offset) {
+    const int64_t Kp = (K + 7) / 8 * 8;
+    const size_t a_bytes = (static_cast<size_t>(M) * Kp * 2 + 255) / 256 * 256;
+    if (b_offset) *b_offset = a_bytes;
+    return a_bytes + (static_cast<size_t>(N) * Kp * 2 + 255) / 256 * 256;
+}
+
+// `allow_repack` = false plans the path that needs no scratch memory.
 Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, const void* out, int stages,
-               int num_sms, unsigned flags) {
+               int num_sms, unsigned flags, bool allow_repack = true) {
     Plan pl;
     const uintptr_t a = reinterpret_cast<uintptr_t>(lhs), b = reinterpret_cast<uintptr_t>(rhs);
     const uintptr_t o = reinterpret_cast<uintptr_t>(out);
-    const bool tma_ok = !(flags & GEMM_DEBUG_FORCE_COPY_PRODUCER) && K % 8 == 0 && a % 16 == 0 && b % 16 == 0;
-    if (tma_ok) {
+    const bool force_copy = flags & GEMM_DEBUG_FORCE_COPY_PRODUCER;
+    const bool native_tma = K % 8 == 0 && a % 16 == 0 && b % 16 == 0;
+    if (!force_copy && native_tma) {
+        pl.producer = kProducerTma;
+        pl.copy_bytes = 16;
+    } else if (!force_copy && allow_repack) {
+        pl.repack = true;
         pl.producer = kProducerTma;
         pl.copy_bytes = 16;
     } else {
@@ -700,7 +759,7 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
     plan[1] = 128 * pl.cg;
     plan[2] = BK;
     plan[3] = pl.cg;
-    plan[4] = pl.producer;
+    plan[4] = pl.repack ? 2 : pl.producer;
     plan[5] = pl.copy_bytes;
     plan[6] = pl.store;
     plan[7] = pl.smem;
@@ -727,19 +786,56 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
     }
     const unsigned flags = debug_flags();
-    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+
+    // Operands whose rows TMA cannot address are first copied to 16-byte
+    // aligned rows in pooled scratch memory; without scratch, the cp.async
+    // producer reads them where they are.
+    const void* a_src = lhs;
+    const void* b_src = rhs;
+    int64_t ld = K;
+    void* scratch = nullptr;
+    if (pl.repack) {
+        size_t b_off = 0;
+        const size_t bytes = repack_bytes(M, N, K, &b_off);
+        scratch = scratch_alloc(info, bytes, stream);
+        if (scratch) {
+            const int64_t Kp = (K + 7) / 8 * 8;
+            uint16_t* da = static_cast<uint16_t*>(scratch);
+            uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
+            const int pairs = K % 2 == 0 && reinterpret_cast<uintptr_t>(lhs) % 4 == 0 &&
+                              reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
+            const int64_t total = (M + N) * (Kp / 8);
+            const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
+            repack_rows_kernel<<<blocks, 256, 0, stream>>>(lhs, M, rhs, N, static_cast<int>(K), static_cast<int>(Kp),
+                                                           da, db, pairs);
+            if (cudaGetLastError() != cudaSuccess) {
+                scratch_free(scratch, stream);
+                return GEMM_ERR_LAUNCH;
+            }
+            a_src = da;
+            b_src = db;
+            ld = Kp;
+        } else {
+            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, false);
+        }
+    }
 
     CUtensorMap ta, tb, tc;
     memset(&ta, 0, sizeof(ta));
     memset(&tb, 0, sizeof(tb));
     memset(&tc, 0, sizeof(tc));
+    auto done = [&](int status) {
+        scratch_free(scratch, stream);       // stream-ordered: after the GEMM has read it
+        return status;
+    };
     if (pl.producer == kProducerTma) {
-        if (!encode_tmap_f16_2d(&ta, lhs, K, M, K * 2, BK, BM_CTA) ||
-            !encode_tmap_f16_2d(&tb, rhs, K, N, K * 2, BK, BN_CTA))
-            return GEMM_ERR_LAUNCH;
+        if (!encode_tmap_f16_2d(&ta, a_src, K, M, ld * 2, BK, BM_CTA) ||
+            !encode_tmap_f16_2d(&tb, b_src, K, N, ld * 2, BK, BN_CTA))
+            return done(GEMM_ERR_LAUNCH);
     }
     if (pl.store == kStoreTma) {
-        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return GEMM_ERR_LAUNCH;
+        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return done(GEMM_ERR_LAUNCH);
     }
     Params p;
     p.M = static_cast<int>(M);
@@ -758,6 +854,6 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     p.rhs = reinterpret_cast<const __half*>(rhs);
     p.out = reinterpret_cast<__half*>(out);
     p.status = info.status;
-    if (pl.cg == 2) return launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream);
-    return launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream);
+    if (pl.cg == 2) return done(launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream));
+    return done(launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream));
 }

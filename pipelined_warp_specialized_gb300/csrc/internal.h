@@ -42,6 +42,13 @@ int sm_count_or_default();
 bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// Stream-ordered scratch memory from a library-owned memory pool of the
+// current device (kept across calls: its release threshold is unlimited, so
+// after the first call of a given size no memory is requested from the
+// driver).  Returns nullptr if the pool cannot provide `bytes`.
+void* scratch_alloc(const DeviceInfo& info, size_t bytes, cudaStream_t stream);
+void scratch_free(void* p, cudaStream_t stream);
+
 // True if [a, a+an) and [b, b+bn) (bytes) intersect.
 inline bool ranges_overlap(const void* a, uint64_t an, const void* b, uint64_t bn) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);

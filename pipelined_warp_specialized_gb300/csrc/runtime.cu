@@ -93,6 +93,45 @@ int sm_count_or_default() {
     return 152;
 }
 
+namespace {
+cudaMemPool_t g_pool[kMaxDevices] = {};
+bool g_pool_tried[kMaxDevices] = {};
+}  // namespace
+
+void* scratch_alloc(const DeviceInfo& info, size_t bytes, cudaStream_t stream) {
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_pool_tried[info.device]) {
+            g_pool_tried[info.device] = true;
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = info.device;
+            cudaMemPool_t p = nullptr;
+            if (cudaMemPoolCreate(&p, &props) == cudaSuccess) {
+                uint64_t keep = ~0ull;      // never hand freed blocks back to the driver
+                cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+                g_pool[info.device] = p;
+            } else {
+                cudaGetLastError();
+            }
+        }
+        pool = g_pool[info.device];
+    }
+    if (!pool) return nullptr;
+    void* ptr = nullptr;
+    if (cudaMallocFromPoolAsync(&ptr, bytes, pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return ptr;
+}
+
+void scratch_free(void* p, cudaStream_t stream) {
+    if (p) cudaFreeAsync(p, stream);
+}
+
 bool encode_tmap_f16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
     EncodeTiledFn fn = encode_fn();

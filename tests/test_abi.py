@@ -87,27 +87,49 @@ def test_plan_headline_shapes(lib):
         assert {k: v for k, v in q.items() if k != "smem_bytes"} == {k: v for k, v in p.items() if k != "smem_bytes"}
 
 
-def test_plan_ragged_shape_uses_copy_producer(lib):
-    # K = 2050: rows of 4100 bytes are not 16-byte aligned, so no TMA descriptor exists
+def test_plan_ragged_shape(lib):
+    # K = 2050: rows of 4100 bytes are not 16-byte aligned, so no TMA descriptor
+    # exists for the operands as given: they are repacked, then fed by TMA
     p = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
-    assert p["producer"] == 1 and p["copy_bytes"] == 4
-    assert p["cta_group"] == 1 and p["bm"] == 128
+    assert p["producer"] == 2 and p["copy_bytes"] == 16
+    assert p["cta_group"] == 2 and p["bm"] == 256               # 16 x 12 pair tiles >= 152 / 2
     assert p["store"] == 0                      # 6000-byte output rows are 16-byte aligned
-    assert p["tiles"] == 32 * 24 and p["k_blocks"] == 33
+    assert p["tiles"] == 16 * 12 and p["k_blocks"] == 33
+    # the async-copy producer reads them in place (single-CTA tile, 4-byte copies)
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
+    try:
+        q = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
+    finally:
+        pws.gemm_set_debug_flags(0)
+    assert q["producer"] == 1 and q["copy_bytes"] == 4
+    assert q["cta_group"] == 1 and q["bm"] == 128
+    assert q["tiles"] == 32 * 24 and q["k_blocks"] == 33
 
 
 def test_plan_edge_cases(lib):
-    assert pws.gemm_f16_nt_plan(7, 9, 3)["copy_bytes"] == 2          # odd K: 2-byte copies
+    assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 2            # odd K: repacked
     assert pws.gemm_f16_nt_plan(7, 9, 3)["store"] == 1               # odd N: plain stores
-    assert pws.gemm_f16_nt_plan(64, 64, 12)["copy_bytes"] == 8       # K % 4 == 0, not % 8
-    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 1   # unaligned base
-    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["copy_bytes"] == 2
-    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 8)["copy_bytes"] == 8
+    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 2   # unaligned base
+    assert pws.gemm_f16_nt_plan(64, 64, 16)["producer"] == 0
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
+    try:
+        assert pws.gemm_f16_nt_plan(7, 9, 3)["copy_bytes"] == 2      # odd K: 2-byte copies
+        assert pws.gemm_f16_nt_plan(64, 64, 12)["copy_bytes"] == 8   # K % 4 == 0, not % 8
+        assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["copy_bytes"] == 2
+        assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 8)["copy_bytes"] == 8
+        assert pws.gemm_f16_nt_plan(64, 64, 16)["producer"] == 1     # forced even when aligned
+    finally:
+        pws.gemm_set_debug_flags(0)
     with pytest.raises(pws.GemmError):
         pws.gemm_f16_nt_plan(64, 64, 16, stages=9)
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE)
     try:
         assert pws.gemm_f16_nt_plan(300, 300, 64)["cta_group"] == 2
+        assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 2   # repacked, then TMA
+    finally:
+        pws.gemm_set_debug_flags(0)
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
+    try:
         assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 1   # copy producer: single CTA
     finally:
         pws.gemm_set_debug_flags(0)

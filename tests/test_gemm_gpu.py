@@ -117,9 +117,12 @@ def test_f16_stage_counts_bitwise_identical(flags):
     (1, 1, 1, 0), (1, 1, 8, 0), (5, 3, 64, 0), (128, 128, 64, 0), (129, 130, 72, 0),
     (260, 300, 136, pws.GEMM_DEBUG_FORCE_PAIR_TILE),      # second pair row: the peer CTA is all padding
     (513, 257, 200, pws.GEMM_DEBUG_FORCE_PAIR_TILE),
-    (65, 70, 33, 0),                                     # odd K: 2-byte element copies
-    (96, 80, 34, 0),                                     # K % 4 == 2: 4-byte copies
-    (96, 80, 44, 0),                                     # K % 8 == 4: 8-byte copies
+    (65, 70, 33, 0),                                     # odd K: repacked, then TMA
+    (96, 80, 34, 0),
+    (65, 70, 33, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER),    # odd K: 2-byte element copies
+    (96, 80, 34, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER),    # K % 4 == 2: 4-byte copies
+    (96, 80, 44, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER),    # K % 8 == 4: 8-byte copies
+    (700, 600, 2050, pws.GEMM_DEBUG_FORCE_PAIR_TILE),    # repacked into the pair tile
     (100, 77, 64, 0),                                    # odd N: guarded plain stores
     (200, 136, 128, pws.GEMM_DEBUG_FORCE_DIRECT_STORE),
     (300, 280, 512, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER | pws.GEMM_DEBUG_FORCE_DIRECT_STORE),
@@ -140,13 +143,18 @@ def test_f16_k_zero_and_empty():
     assert out.shape == (0, 4)
 
 
-def test_f16_unaligned_operands():
+@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER], ids=["repack", "copy"])
+def test_f16_unaligned_operands(flags):
     M, N, K = 150, 90, 128
     big_a = _dev(inputs.uniform_f16(5, 0, (M * K + 1,)))
     a_t = big_a[1:].view(M, K)                           # 2-byte aligned only
     b = inputs.uniform_f16(5, 1, (N, K))
-    out = pws.gemm_f16_nt(a_t, _dev(b), stages=2)
-    torch.cuda.synchronize()
+    pws.gemm_set_debug_flags(flags)
+    try:
+        out = pws.gemm_f16_nt(a_t, _dev(b), stages=2)
+        torch.cuda.synchronize()
+    finally:
+        pws.gemm_set_debug_flags(0)
     assert pws.gemm_device_status() == pws.GEMM_OK
     assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b), K)
 
@@ -204,10 +212,34 @@ def test_f16_4096_config_sampled():
 
 
 def test_f16_ragged_config_full():
+    # K = 2050: the default path repacks the operands and runs the TMA pair
+    # tile; the async-copy producer reads them in place.  Both against the oracle.
     wl = inputs.WORKLOADS["f16_nt_ragged_4000x3000x2050"]
     a, b = wl.lhs(), wl.rhs()
-    assert pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K)["producer"] == 1
-    assert_f16_ok(run_f16(a, b, 3), oracle.gemm_f16_nt_f64(a, b), wl.K)
+    assert pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K)["producer"] == 2
+    ref = oracle.gemm_f16_nt_f64(a, b)
+    assert_f16_ok(run_f16(a, b, 3), ref, wl.K)
+    assert_f16_ok(run_f16(a, b, 3, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER), ref, wl.K)
+
+
+def test_f16_repack_scratch_is_stream_ordered():
+    # two unaligned-K GEMMs in flight on two streams, each with its own pooled
+    # scratch, repeated so the pool hands blocks back and out again
+    M, N, K = 640, 520, 1030
+    cases = []
+    for seed in (41, 42):
+        a = inputs.uniform_f16(seed, 0, (M, K))
+        b = inputs.uniform_f16(seed, 1, (N, K))
+        cases.append((a, b, _dev(a), _dev(b), oracle.gemm_f16_nt_f64(a, b)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty(M, N, dtype=torch.float16, device="cuda") for _ in range(2)]
+    for _ in range(3):
+        for (a, b, da, db, _), s, o in zip(cases, streams, outs):
+            pws.gemm_f16_nt(da, db, o, stages=4, stream=s)
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_OK
+        for (a, b, da, db, ref), o in zip(cases, outs):
+            assert_f16_ok(o.cpu().numpy(), ref, K)
 
 
 def test_f16_8192_sweep_identical_across_stages():
