@@ -78,7 +78,10 @@ constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
 constexpr int MAX_STAGES = 6;
 constexpr int COPY_WARPS = 8;          // producer warps of the cp.async producer
 constexpr int COPY_THREADS = COPY_WARPS * 32;
-constexpr int GROUP_M = 8;             // tile-row group height of the raster order
+#ifndef PWS_GROUP_M
+#define PWS_GROUP_M 8
+#endif
+constexpr int GROUP_M = PWS_GROUP_M;   // tile-row group height of the raster order
 
 enum { kProducerTma = 0, kProducerCopy = 1 };
 enum { kStoreTma = 0, kStoreDirect = 1 };
