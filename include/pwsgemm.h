@@ -115,6 +115,33 @@ int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const ge
                 gemm_f16_t* out, int stages, cudaStream_t stream);
 
 /*
+ * gemm_f16_nt_noalloc -- gemm_f16_nt for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point.
+ *
+ * Same arguments, layouts, results and return codes as gemm_f16_nt.  Where
+ * gemm_f16_nt takes scratch from its memory pool (operands whose rows the
+ * tensor memory accelerator cannot address), this call uses a fixed 32 MiB
+ * array in device memory that exists from the moment the library is loaded
+ * until the process exits, on every GPU that loads it.  It never asks the
+ * driver or any allocator for memory, which suits code running under a
+ * fixed device-memory budget, code that has reserved all device memory up
+ * front, and code that must not enter an allocator (which may synchronize or
+ * fail at a point the caller cannot handle).
+ *   - Scratch needed: round256(M*Kp*2) + round256(N*Kp*2) bytes, Kp = K
+ *     rounded up to a multiple of 8.  Above 32 MiB (33554432 bytes) the call
+ *     returns GEMM_ERR_INVALID_ARG without launching anything.  Operands the
+ *     accelerator can address directly need no scratch and have no limit.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array.  Calls that can overlap on the GPU (on
+ *     streams with no ordering between them) race on it: order them.  The
+ *     array keeps the last call's contents; each call overwrites every byte
+ *     it reads, so nothing needs clearing.
+ */
+int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
+                        gemm_f16_t* out, int stages, cudaStream_t stream);
+
+/*
  * gemm_device_status -- synchronizes `stream`, then returns and clears the
  * device status word of the current device: GEMM_OK, or GEMM_ERR_TIMEOUT if a
  * bounded wait inside any kernel of this library expired since the last call.

@@ -59,6 +59,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gemm_s32_nn.restype = i32
     lib.gemm_f16_nt.argtypes = [i64, i64, i64, vp, vp, vp, i32, vp]
     lib.gemm_f16_nt.restype = i32
+    lib.gemm_f16_nt_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, i32, vp]
+    lib.gemm_f16_nt_noalloc.restype = i32
     lib.gemm_device_status.argtypes = [vp]
     lib.gemm_device_status.restype = i32
     lib.gemm_status_string.argtypes = [i32]
@@ -139,6 +141,36 @@ def gemm_f16_nt(lhs, rhs, out=None, stages: int = 4, stream=None):
     with torch.cuda.device(lhs.device):
         _check(load_library().gemm_f16_nt(M, N, K, lhs.data_ptr(), rhs.data_ptr(), out.data_ptr(), int(stages),
                                           _stream_ptr(stream, lhs.device)), "gemm_f16_nt")
+    return out
+
+
+def gemm_f16_nt_noalloc(lhs, rhs, out=None, stages: int = 4, stream=None):
+    """gemm_f16_nt for callers that cannot allocate device memory.
+
+    Where gemm_f16_nt would take scratch from its pool, this uses a fixed
+    32 MiB device array loaded with the library, so no allocator is entered
+    (for code under a fixed memory budget or that must not allocate).  Calls
+    share that array: calls that can overlap on the GPU must be ordered.
+    Raises GemmError(GEMM_ERR_INVALID_ARG) when more scratch would be needed.
+    ``out`` should be preallocated by such callers (None allocates it here).
+    """
+    import torch
+    if lhs.dtype != torch.float16 or rhs.dtype != torch.float16:
+        raise TypeError("gemm_f16_nt_noalloc takes float16 tensors")
+    if lhs.dim() != 2 or rhs.dim() != 2 or lhs.shape[1] != rhs.shape[1]:
+        raise ValueError(f"shapes {tuple(lhs.shape)} x {tuple(rhs.shape)} do not form [M,K] x [N,K]")
+    if not (lhs.is_cuda and rhs.is_cuda) or not lhs.is_contiguous() or not rhs.is_contiguous():
+        raise ValueError("gemm_f16_nt_noalloc takes contiguous CUDA tensors")
+    M, K = lhs.shape
+    N = rhs.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=lhs.device)
+    elif out.shape != (M, N) or out.dtype != torch.float16 or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous float16 CUDA tensor of shape [M, N]")
+    with torch.cuda.device(lhs.device):
+        _check(load_library().gemm_f16_nt_noalloc(M, N, K, lhs.data_ptr(), rhs.data_ptr(), out.data_ptr(),
+                                                  int(stages), _stream_ptr(stream, lhs.device)),
+               "gemm_f16_nt_noalloc")
     return out
 
 

@@ -53,6 +53,7 @@
 #include <cstdint>
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -859,4 +860,126 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     p.status = info.status;
     if (pl.cg == 2) return done(launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream));
     return done(launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream));
+}
+
+// ---------------------------------------------------------------- no-allocation variant
+//
+// gemm_f16_nt gets the scratch of its repack step (operands whose rows the
+// tensor memory accelerator cannot address) from a memory pool, which may
+// have to ask the driver for memory.  Some callers cannot allow that: code
+// running under a fixed device-memory budget that must not grow, code that
+// must not call into the allocator at all (it can synchronise or fail at a
+// point the caller cannot handle), or code that has reserved all device
+// memory up front.  gemm_f16_nt_noalloc serves them with scratch that exists
+// from the moment the library is loaded: a fixed array in device memory.
+namespace pws {
+namespace f16nt {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;   // 32 MiB
+
+// The scratch array.  Every GPU that loads this library holds it until the
+// process exits.  In host code its name only stands in for the symbol: it is
+// not a device address, and passing it to a kernel would fault (or, where the
+// GPU can reach host memory, silently use the wrong memory).  The device
+// address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of the scratch array on `device` (the current device).
+// The first call per device looks it up; returns nullptr on failure.
+void* noalloc_scratch(int device) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (device < 0 || device >= 64) return nullptr;
+    if (!g_noalloc_addr[device]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_addr[device] = p;
+    }
+    return g_noalloc_addr[device];
+}
+
+}  // namespace f16nt
+}  // namespace pws
+
+extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
+                                   gemm_f16_t* out, int stages, cudaStream_t stream) {
+    using namespace pws;
+    using namespace pws::f16nt;
+    int rc = validate(M, N, K, lhs, rhs, out, stages);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceInfo info;
+    rc = current_device(&info);
+    if (rc != GEMM_OK) return rc;
+    if (K == 0) {
+        const int64_t n = M * N;
+        int blocks = static_cast<int>((n + 255) / 256);
+        if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
+        zero_fill_u16<<<blocks, 256, 0, stream>>>(reinterpret_cast<unsigned short*>(out), n);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+    const unsigned flags = debug_flags();
+    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+
+    const void* a_src = lhs;
+    const void* b_src = rhs;
+    int64_t ld = K;
+    if (pl.repack) {
+        size_t b_off = 0;
+        if (repack_bytes(M, N, K, &b_off) > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
+        void* scratch = noalloc_scratch(info.device);
+        if (!scratch) return GEMM_ERR_LAUNCH;
+        // The repack writes every scratch byte the GEMM then reads (padding
+        // included), so nothing left over from an earlier call is ever used.
+        const int64_t Kp = (K + 7) / 8 * 8;
+        uint16_t* da = static_cast<uint16_t*>(scratch);
+        uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
+        const int pairs = K % 2 == 0 && reinterpret_cast<uintptr_t>(lhs) % 4 == 0 &&
+                          reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
+        const int64_t total = (M + N) * (Kp / 8);
+        const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
+        repack_rows_kernel<<<blocks, 256, 0, stream>>>(lhs, M, rhs, N, static_cast<int>(K), static_cast<int>(Kp), da,
+                                                       db, pairs);
+        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+        a_src = da;
+        b_src = db;
+        ld = Kp;
+    }
+
+    CUtensorMap ta, tb, tc;
+    memset(&ta, 0, sizeof(ta));
+    memset(&tb, 0, sizeof(tb));
+    memset(&tc, 0, sizeof(tc));
+    if (pl.producer == kProducerTma) {
+        if (!encode_tmap_f16_2d(&ta, a_src, K, M, ld * 2, BK, BM_CTA) ||
+            !encode_tmap_f16_2d(&tb, b_src, K, N, ld * 2, BK, BN_CTA))
+            return GEMM_ERR_LAUNCH;
+    }
+    if (pl.store == kStoreTma) {
+        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return GEMM_ERR_LAUNCH;
+    }
+    Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = pl.num_kb;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.num_tiles;
+    p.producer = pl.producer;
+    p.copy_bytes = pl.copy_bytes;
+    p.store = pl.store;
+    p.flags = flags;
+    p.timeout_ns = wait_timeout_ns();
+    p.lhs = reinterpret_cast<const __half*>(lhs);
+    p.rhs = reinterpret_cast<const __half*>(rhs);
+    p.out = reinterpret_cast<__half*>(out);
+    p.status = info.status;
+    if (pl.cg == 2) return launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream);
+    return launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream);
 }
