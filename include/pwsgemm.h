@@ -79,6 +79,25 @@ int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32
                 int32_t* out, cudaStream_t stream);
 
 /*
+ * gemm_s32_nn_ring -- gemm_s32_nn with an S-slot ring instead of two buffers.
+ *
+ * Croqtile tutorial ch.6, section "swap：交换的是名称，不是字节" (rotate(f0, f1,
+ * f2) over three buffers, generalised to S) and the CUDA tutorial ch.4,
+ * section 4.8.3 (a pipeline that fills S - 1 slots before its main loop).
+ * The prologue issues K tiles 0..S-2; iteration t issues tile t+S-1 into the
+ * slot tile t-1 vacated, waits for tile t, multiplies it.  S - 1 tiles are in
+ * flight while one is multiplied.
+ *
+ *   Arguments, layouts and wrapping arithmetic as gemm_s32_nn; the result is
+ *   bit-identical to it.  stages : S, 2..6 (2 is the double buffer).
+ *
+ * Returns the codes of gemm_s32_nn, or GEMM_ERR_UNSUPPORTED_STAGES for S
+ * outside 2..6.
+ */
+int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32_t* rhs,
+                     int32_t* out, int stages, cudaStream_t stream);
+
+/*
  * gemm_f16_nt -- out[M,N] = f16( lhs[M,K] . rhs[N,K]^T ), fp32 accumulation.
  *
  * Croqtile tutorial ch.6, section "带 event 的 1P1C 内核" (lhs declared

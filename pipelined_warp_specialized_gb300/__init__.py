@@ -57,6 +57,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     i64, i32, vp, u32, u64 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint, ctypes.c_uint64
     lib.gemm_s32_nn.argtypes = [i64, i64, i64, vp, vp, vp, vp]
     lib.gemm_s32_nn.restype = i32
+    lib.gemm_s32_nn_ring.argtypes = [i64, i64, i64, vp, vp, vp, i32, vp]
+    lib.gemm_s32_nn_ring.restype = i32
     lib.gemm_f16_nt.argtypes = [i64, i64, i64, vp, vp, vp, i32, vp]
     lib.gemm_f16_nt.restype = i32
     lib.gemm_f16_nt_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, i32, vp]
@@ -120,6 +122,27 @@ def gemm_s32_nn(lhs, rhs, out=None, stream=None):
     with torch.cuda.device(lhs.device):
         _check(load_library().gemm_s32_nn(M, N, K, lhs.data_ptr(), rhs.data_ptr(), out.data_ptr(),
                                           _stream_ptr(stream, lhs.device)), "gemm_s32_nn")
+    return out
+
+
+def gemm_s32_nn_ring(lhs, rhs, out=None, stages: int = 4, stream=None):
+    """gemm_s32_nn with an S-slot ring (S = `stages`, 2..6); bit-identical results."""
+    import torch
+    if lhs.dtype != torch.int32 or rhs.dtype != torch.int32:
+        raise TypeError("gemm_s32_nn_ring takes int32 tensors")
+    if lhs.dim() != 2 or rhs.dim() != 2 or lhs.shape[1] != rhs.shape[0]:
+        raise ValueError(f"shapes {tuple(lhs.shape)} x {tuple(rhs.shape)} do not form [M,K] x [K,N]")
+    if not (lhs.is_cuda and rhs.is_cuda) or not lhs.is_contiguous() or not rhs.is_contiguous():
+        raise ValueError("gemm_s32_nn_ring takes contiguous CUDA tensors")
+    M, K = lhs.shape
+    N = rhs.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=lhs.device)
+    elif out.shape != (M, N) or out.dtype != torch.int32 or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous int32 CUDA tensor of shape [M, N]")
+    with torch.cuda.device(lhs.device):
+        _check(load_library().gemm_s32_nn_ring(M, N, K, lhs.data_ptr(), rhs.data_ptr(), out.data_ptr(), int(stages),
+                                               _stream_ptr(stream, lhs.device)), "gemm_s32_nn_ring")
     return out
 
 

@@ -178,3 +178,176 @@ extern "C" int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, 
         e = s32nn::launch_tile<16, 16, 1, 1>((int)M, (int)N, (int)K, lhs, rhs, out, a16, b16, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
 }
+
+// ---------------------------------------------------------------- S-slot ring
+//
+// The same product with S shared-memory slots instead of two: the Croqtile
+// tutorial ch.6 generalises swap(f0, f1) to rotate(f0, f1, f2) for three
+// buffers ("swap：交换的是名称，不是字节"), and the CUDA tutorial ch.4,
+// section 4.8.3 fills S - 1 slots before its main loop.  Here the prologue
+// issues tiles 0 .. S-2; iteration t issues tile t + S - 1 into the slot tile
+// t - 1 vacated, waits until tile t has landed (cp.async.wait_group S - 1,
+// then __syncthreads), multiplies slot t mod S and synchronises again before
+// that slot is refilled.  Rotating the slot index is rotate() over S handles.
+// With S tiles in flight the load latency of the small page-size problem is
+// paid about T / (S - 1) times instead of T times; results are bit-identical
+// to the two-buffer kernel (same products, same order, exact arithmetic).
+namespace pws {
+namespace s32nn {
+
+// cp.async.wait_group with a run-time count (the instruction takes an immediate).
+__device__ __forceinline__ void cp_async_wait_upto(int pending) {
+    switch (pending) {
+        case 0: cp_async_wait_group<0>(); break;
+        case 1: cp_async_wait_group<1>(); break;
+        case 2: cp_async_wait_group<2>(); break;
+        case 3: cp_async_wait_group<3>(); break;
+        case 4: cp_async_wait_group<4>(); break;
+        default: cp_async_wait_group<5>(); break;
+    }
+}
+
+template <int BM, int BN, int TM, int TN, int CBYTES>
+__global__ void __launch_bounds__(THREADS)
+gemm_s32_nn_ring_kernel(int M, int N, int K, int S, const int32_t* __restrict__ lhs,
+                        const int32_t* __restrict__ rhs, int32_t* __restrict__ out) {
+    static_assert((BM / TM) * (BN / TN) == THREADS, "one thread per TM x TN block");
+    constexpr int A_WORDS = BM * (BK + APAD);      // one slot of A: [BM][BK + APAD]
+    constexpr int B_WORDS = BK * BN;               // one slot of B: [BK][BN]
+    extern __shared__ __align__(16) int32_t ring[];
+    int32_t* const As = ring;
+    int32_t* const Bs = ring + S * A_WORDS;
+
+    const int tid = threadIdx.x;
+    const int tx = tid % (BN / TN);
+    const int ty = tid / (BN / TN);
+    const int m0 = blockIdx.y * BM;
+    const int n0 = blockIdx.x * BN;
+    const int T = (K + BK - 1) / BK;
+
+    auto issue = [&](int t, int slot) {
+        const int k0 = t * BK;
+        constexpr int E = CBYTES / 4;
+        int32_t* a = As + slot * A_WORDS;
+        int32_t* b = Bs + slot * B_WORDS;
+        for (int i = tid; i < BM * (BK / E); i += THREADS) {
+            const int r = i / (BK / E), c = (i % (BK / E)) * E;
+            const int gm = m0 + r, gk = k0 + c;
+            const bool ok = gm < M && gk < K;
+            cp_async<CBYTES>(smem_u32(a + r * (BK + APAD) + c), ok ? lhs + (int64_t)gm * K + gk : lhs, ok ? CBYTES : 0);
+        }
+        for (int i = tid; i < BK * (BN / E); i += THREADS) {
+            const int r = i / (BN / E), c = (i % (BN / E)) * E;
+            const int gk = k0 + r, gn = n0 + c;
+            const bool ok = gk < K && gn < N;
+            cp_async<CBYTES>(smem_u32(b + r * BN + c), ok ? rhs + (int64_t)gk * N + gn : rhs, ok ? CBYTES : 0);
+        }
+    };
+
+    uint32_t acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0u;
+
+    // prologue: S - 1 tiles in flight
+    for (int t = 0; t < S - 1; ++t) {
+        if (t < T) issue(t, t);
+        cp_async_commit();
+    }
+    for (int t = 0; t < T; ++t) {
+        const int nt = t + S - 1;
+        if (nt < T) issue(nt, nt % S);       // the slot tile t - 1 vacated
+        cp_async_commit();
+        cp_async_wait_upto(S - 1);           // tile t has landed ...
+        __syncthreads();                     // ... and is visible to all threads
+        const int32_t* a = As + (t % S) * A_WORDS;
+        const int32_t* b = Bs + (t % S) * B_WORDS;
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+            uint32_t av[TM], bv[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) av[i] = static_cast<uint32_t>(a[(ty * TM + i) * (BK + APAD) + k]);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) bv[j] = static_cast<uint32_t>(b[k * BN + tx * TN + j]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] += av[i] * bv[j];
+        }
+        __syncthreads();                     // slot t mod S is free for tile t + S
+    }
+    cp_async_wait_group<0>();
+
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int gm = m0 + ty * TM + i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int gn = n0 + tx * TN + j;
+            if (gn < N) out[(int64_t)gm * N + gn] = static_cast<int32_t>(acc[i][j]);
+        }
+    }
+}
+
+template <int BM, int BN, int TM, int TN>
+cudaError_t launch_ring(int M, int N, int K, int S, const int32_t* lhs, const int32_t* rhs, int32_t* out,
+                        bool vec16, int device, cudaStream_t stream) {
+    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+    const size_t smem = static_cast<size_t>(S) * (BM * (BK + APAD) + BK * BN) * sizeof(int32_t);
+    static bool configured16[64] = {}, configured4[64] = {};
+    if (vec16) {
+        auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, 16>;
+        if (!configured16[device]) {
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 6 * (BM * (BK + APAD) + BK * BN) * 4) != cudaSuccess)
+                return cudaGetLastError();
+            configured16[device] = true;
+        }
+        k<<<grid, THREADS, smem, stream>>>(M, N, K, S, lhs, rhs, out);
+    } else {
+        auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, 4>;
+        if (!configured4[device]) {
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 6 * (BM * (BK + APAD) + BK * BN) * 4) != cudaSuccess)
+                return cudaGetLastError();
+            configured4[device] = true;
+        }
+        k<<<grid, THREADS, smem, stream>>>(M, N, K, S, lhs, rhs, out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace s32nn
+}  // namespace pws
+
+extern "C" int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32_t* rhs,
+                                int32_t* out, int stages, cudaStream_t stream) {
+    using namespace pws;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
+    if (stages < 2 || stages > 6) return GEMM_ERR_UNSUPPORTED_STAGES;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!out || (K > 0 && (!lhs || !rhs))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lhs) |
+         reinterpret_cast<uintptr_t>(rhs)) & 3u)
+        return GEMM_ERR_ALIGNMENT;
+    const uint64_t out_b = (uint64_t)M * N * 4;
+    if (K > 0 && (ranges_overlap(out, out_b, lhs, (uint64_t)M * K * 4) ||
+                  ranges_overlap(out, out_b, rhs, (uint64_t)K * N * 4)))
+        return GEMM_ERR_INVALID_ARG;
+    DeviceInfo info;
+    const int rc = current_device(&info);
+    if (rc != GEMM_OK) return rc;
+    // 16-byte copies need 16-byte aligned rows on both sides, else one element per copy
+    const bool vec16 = (K % 4 == 0) && (N % 4 == 0) && (reinterpret_cast<uintptr_t>(lhs) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(rhs) % 16 == 0);
+    auto blocks = [&](int bm, int bn) { return ((M + bm - 1) / bm) * ((N + bn - 1) / bn); };
+    cudaError_t e;
+    if (blocks(64, 64) >= info.num_sms)
+        e = s32nn::launch_ring<64, 64, 4, 4>((int)M, (int)N, (int)K, stages, lhs, rhs, out, vec16, info.device, stream);
+    else if (blocks(32, 32) >= info.num_sms)
+        e = s32nn::launch_ring<32, 32, 2, 2>((int)M, (int)N, (int)K, stages, lhs, rhs, out, vec16, info.device, stream);
+    else
+        e = s32nn::launch_ring<16, 16, 1, 1>((int)M, (int)N, (int)K, stages, lhs, rhs, out, vec16, info.device, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+}

@@ -67,6 +67,17 @@ def test_s32_argument_checks_return_before_launch(lib, args, want):
     assert lib.gemm_s32_nn(*args, None) == want
 
 
+@pytest.mark.parametrize("args,want", [
+    ((4, 4, 4, A, B, C, 1), pws.GEMM_ERR_UNSUPPORTED_STAGES),
+    ((4, 4, 4, A, B, C, 7), pws.GEMM_ERR_UNSUPPORTED_STAGES),
+    ((-1, 4, 4, A, B, C, 3), pws.GEMM_ERR_INVALID_ARG),
+    ((4, 4, 4, A + 2, B, C, 3), pws.GEMM_ERR_ALIGNMENT),
+    ((0, 4, 4, 0, 0, 0, 3), pws.GEMM_OK),
+])
+def test_s32_ring_argument_checks_return_before_launch(lib, args, want):
+    assert lib.gemm_s32_nn_ring(*args, None) == want
+
+
 def test_debug_flags_and_timeout_setters(lib):
     assert lib.gemm_set_debug_flags(1 << 10) == pws.GEMM_ERR_INVALID_ARG
     assert lib.gemm_set_debug_flags(0) == pws.GEMM_OK

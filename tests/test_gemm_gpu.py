@@ -73,6 +73,21 @@ def test_s32_shapes_bit_exact(M, N, K):
     assert np.array_equal(run_s32(a, b), oracle.gemm_s32_nn(a, b))
 
 
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (1, 1, 1), (17, 33, 15), (300, 500, 77), (1000, 1000, 1000),
+                                   (33, 18, 130)])
+def test_s32_ring_every_stage_count_bit_exact(M, N, K):
+    a = inputs.ints(M + 11, 0, (M, K), -1000, 1000)
+    b = inputs.ints(N + 13, 1, (K, N), -1000, 1000)
+    want = oracle.gemm_s32_nn(a, b)
+    da, db = _dev(a), _dev(b)
+    two = pws.gemm_s32_nn(da, db)
+    for s in range(2, 7):
+        got = pws.gemm_s32_nn_ring(da, db, stages=s)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), want), f"S={s}"
+        assert torch.equal(got, two)
+
+
 def test_s32_wraps_on_overflow():
     M, N, K = 40, 24, 64
     a = inputs.ints(1, 0, (M, K), -2**31, 2**31 - 1)
