@@ -182,6 +182,35 @@ def time_launches(fn, steps, warmup, torch, stream):
     return e0.elapsed_time(e1) / steps
 
 
+def time_graph(fn, torch, per_graph=20, replays=20):
+    """Average ms per launch of fn(stream), replayed from a CUDA graph.
+
+    For launch-bound small problems: the graph removes the host-side cost of
+    each call (Python, ctypes, argument checks), leaving the GPU time.
+    """
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn(s)                       # first calls do the per-device set-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(per_graph):
+            fn(s)
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(replays):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (replays * per_graph)
+
+
 def e2e_pipelined(pws, torch, dev, a_h, b_h, c_h, stages, n_steps, warmup=2):
     """Average ms per step of host -> device -> GEMM -> host, pipelined over steps.
 
@@ -243,12 +272,14 @@ def extra_configs(pws, torch, stream, reps=20):
     a = torch.from_numpy(wl.lhs()).to(dev)
     b = torch.from_numpy(wl.rhs()).to(dev)
     c = torch.empty(wl.M, wl.N, dtype=torch.int32, device=dev)
-    ms = time_launches(lambda: pws.gemm_s32_nn(a, b, c, stream=stream), 200, 20, torch, stream)
+    ms_eager = time_launches(lambda: pws.gemm_s32_nn(a, b, c, stream=stream), 200, 20, torch, stream)
+    ms = time_graph(lambda st: pws.gemm_s32_nn(a, b, c, stream=st), torch)
     out[wl.name] = {"us": round(ms * 1e3, 2), "TOPS": round(wl.flops / ms / 1e9, 3),
-                    "GB_s": round((wl.M * wl.K + wl.K * wl.N + wl.M * wl.N) * 4 / ms / 1e6, 1)}
+                    "GB_s": round((wl.M * wl.K + wl.K * wl.N + wl.M * wl.N) * 4 / ms / 1e6, 1),
+                    "us_eager": round(ms_eager * 1e3, 2), "timing": "CUDA-graph replay (us), eager calls (us_eager)"}
     ring = {}
     for s in range(2, 7):
-        ms = time_launches(lambda: pws.gemm_s32_nn_ring(a, b, c, stages=s, stream=stream), 200, 20, torch, stream)
+        ms = time_graph(lambda st: pws.gemm_s32_nn_ring(a, b, c, stages=s, stream=st), torch)
         ring[f"S{s}"] = {"us": round(ms * 1e3, 2), "TOPS": round(wl.flops / ms / 1e9, 3)}
     out[wl.name + "/ring"] = ring
     for name in ("f16_nt_1024", "f16_nt_4096", "f16_nt_ragged_4000x3000x2050", "f16_nt_8192"):
@@ -268,11 +299,17 @@ def extra_configs(pws, torch, stream, reps=20):
                 label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B", 2: "repack+tma"}[plan["producer"]]
                 res = {"producer": label, "cta_group": plan["cta_group"]}
                 n = reps if wl.M * wl.N * wl.K < 2 ** 36 else max(5, reps // 2)
+                small = wl.flops < 2 ** 34        # launch-bound: time from a CUDA graph
                 for s in wl.stages:
-                    ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3,
-                                       torch, stream)
+                    if small and not plan["producer"] == 2:
+                        ms = time_graph(lambda st: pws.gemm_f16_nt(a, b, c, stages=s, stream=st), torch)
+                    else:
+                        ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3,
+                                           torch, stream)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
                                     "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1)}
+                    if small and not plan["producer"] == 2:
+                        res[f"S{s}"]["timing"] = "CUDA-graph replay"
             finally:
                 pws.gemm_set_debug_flags(0)
             out[name + ("/" + suffix if suffix else "")] = res
