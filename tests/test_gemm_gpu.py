@@ -88,6 +88,37 @@ def test_s32_ring_every_stage_count_bit_exact(M, N, K):
         assert torch.equal(got, two)
 
 
+def test_graph_capture_replays_correctly():
+    # the entry points only enqueue work on the given stream, so they can be
+    # captured into a CUDA graph and replayed
+    wl = inputs.WORKLOADS["s32_nn_128x256x256"]
+    a32, b32 = wl.lhs(), wl.rhs()
+    da32, db32 = _dev(a32), _dev(b32)
+    o32 = torch.empty(wl.M, wl.N, dtype=torch.int32, device="cuda")
+    M, N, K = 520, 384, 320
+    a16 = inputs.uniform_f16(61, 0, (M, K))
+    b16 = inputs.uniform_f16(61, 1, (N, K))
+    da16, db16 = _dev(a16), _dev(b16)
+    o16 = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):                       # first calls outside the capture
+        pws.gemm_s32_nn(da32, db32, o32, stream=s)
+        pws.gemm_f16_nt(da16, db16, o16, stages=3, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pws.gemm_s32_nn(da32, db32, o32, stream=s)
+        pws.gemm_f16_nt(da16, db16, o16, stages=3, stream=s)
+    o32.zero_()
+    o16.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    assert np.array_equal(o32.cpu().numpy(), oracle.gemm_s32_nn(a32, b32))
+    assert_f16_ok(o16.cpu().numpy(), oracle.gemm_f16_nt_f64(a16, b16), K)
+
+
 def test_s32_wraps_on_overflow():
     M, N, K = 40, 24, 64
     a = inputs.ints(1, 0, (M, K), -2**31, 2**31 - 1)
