@@ -126,6 +126,15 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  * operands instead.  Partial tiles are zero-filled on load and clipped on
  * store.
  *
+ * The kernel is persistent: a grid of as many CTA groups as fit on the GPU
+ * strides over the output tiles.  When the tile count leaves a last, partial
+ * wave, each tile of that wave is cut along K into parts that run on the
+ * wave's otherwise idle CTA groups; the parts' fp32 partial sums go to
+ * scratch from the same pool, and the last part to finish adds them in part
+ * order before rounding to f16 (so the result depends on the shape and the
+ * device's SM count, not on S or on timing).  If the pool cannot supply that
+ * scratch the tiles are not cut.
+ *
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT (a pointer not
  * 2-byte aligned), GEMM_ERR_UNSUPPORTED_STAGES, GEMM_ERR_UNSUPPORTED_ARCH or
  * GEMM_ERR_LAUNCH.  M, N, K must each be below 2^31.
@@ -198,6 +207,8 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *       the CTA-pair 256x256 tile would be chosen.
  *   GEMM_DEBUG_FORCE_PAIR_TILE     : use the CTA-pair 256x256 tile whenever the
  *       TMA producer is used, even for small outputs.
+ *   GEMM_DEBUG_NO_SPLIT            : do not split the last wave's tiles along K
+ *       (gemm_f16_nt normally does, see below).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -205,7 +216,8 @@ enum {
     GEMM_DEBUG_FORCE_COPY_PRODUCER = 2u,
     GEMM_DEBUG_FORCE_DIRECT_STORE = 4u,
     GEMM_DEBUG_FORCE_SOLO_TILE = 8u,
-    GEMM_DEBUG_FORCE_PAIR_TILE = 16u
+    GEMM_DEBUG_FORCE_PAIR_TILE = 16u,
+    GEMM_DEBUG_NO_SPLIT = 32u
 };
 int gemm_set_debug_flags(unsigned flags);
 

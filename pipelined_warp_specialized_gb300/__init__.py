@@ -34,6 +34,7 @@ GEMM_DEBUG_FORCE_COPY_PRODUCER = 2
 GEMM_DEBUG_FORCE_DIRECT_STORE = 4
 GEMM_DEBUG_FORCE_SOLO_TILE = 8
 GEMM_DEBUG_FORCE_PAIR_TILE = 16
+GEMM_DEBUG_NO_SPLIT = 32
 
 _lib = None
 

@@ -100,6 +100,13 @@ struct Params {
     const __half* rhs;
     __half* out;
     unsigned* status;
+    // Work units: units 0 .. full_units-1 are whole output tiles (unit = tile).
+    // With split == 2, each remaining tile (those of the last, partial wave)
+    // is cut into two units, its left and right halves of columns, which run
+    // the full K loop with a half-width MMA (no partial sums to combine).
+    int full_units;
+    int split;
+    int total_units;
 };
 
 template <int CG>
@@ -164,6 +171,18 @@ __device__ __forceinline__ void tile_coords(int t, const Params& p, int& tm, int
     const int r = t - g * group;
     tm = first + r % rows;
     tn = r / rows;
+}
+
+// One persistent work unit: an output tile, or (half = 0 or 1) the left or
+// right half of its columns.
+struct Unit {
+    int tile, half;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, const Params& p) {
+    if (p.split < 2 || u < p.full_units) return Unit{u, -1};
+    const int v = u - p.full_units;
+    return Unit{p.full_units + v / 2, v % 2};
 }
 
 // Bounded mbarrier wait.  Returns false if the wait gave up (time limit or
@@ -267,9 +286,10 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
     const int t = threadIdx.x;                   // 0 .. COPY_THREADS - 1
     uint32_t stage = 0, phase = 0, issued = 0, signalled = 0;
     bool ok = true;
-    for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+    for (int u = cluster_id; ok && u < p.total_units; u += num_clusters) {
+        const Unit un = unit_of(u, p);
         int tm, tn;
-        tile_coords(tile, p, tm, tn);
+        tile_coords(un.tile, p, tm, tn);
         for (int kb = 0; kb < p.num_kb; ++kb) {
             bool got = true;
             if (lane == 0) got = W.wait(bEMPTY + 8 * stage, phase);
@@ -301,7 +321,8 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
 template <int CG, int S>
 __global__ void __launch_bounds__((COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
+                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ Params p) {
     using SH = Shape<CG>;
     using L = Layout<S>;
     extern __shared__ uint8_t smem_raw[];
@@ -367,23 +388,29 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 uint32_t stage = 0, phase = 0;
                 uint32_t issued = 0;
                 bool ok = true;
-                for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                for (int u = cluster_id; ok && u < p.total_units; u += num_clusters) {
+                    const Unit un = unit_of(u, p);
                     int tm, tn;
-                    tile_coords(t, p, tm, tn);
+                    tile_coords(un.tile, p, tm, tn);
                     const int m_cta = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA;
-                    const int n_cta = tn * SH::UMMA_N + static_cast<int>(rank) * BN_CTA;
+                    // a half-width unit loads half of the CTA's B rows (tmBh: a 64-row box)
+                    const bool halfw = un.half >= 0;
+                    const int n_cta = halfw ? tn * SH::UMMA_N + un.half * (SH::UMMA_N / 2) + static_cast<int>(rank) * (BN_CTA / 2)
+                                            : tn * SH::UMMA_N + static_cast<int>(rank) * BN_CTA;
+                    const CUtensorMap* tb = halfw ? &tmBh : &tmB;
+                    const uint32_t bytes = halfw ? A_SLOT + B_SLOT / 2 : SLOT_BYTES;
                     for (int kb = 0; kb < p.num_kb; ++kb) {
                         if (!W.wait(bEMPTY + 8 * stage, phase)) { ok = false; break; }
                         const uint32_t a_dst = sA + stage * A_SLOT, b_dst = sB + stage * B_SLOT;
                         if constexpr (CG == 1) {
-                            mbar_arrive_expect_tx(bFULL + 8 * stage, SLOT_BYTES);
+                            mbar_arrive_expect_tx(bFULL + 8 * stage, bytes);
                             tma_load_2d(a_dst, &tmA, kb * BK, m_cta, bFULL + 8 * stage);
-                            tma_load_2d(b_dst, &tmB, kb * BK, n_cta, bFULL + 8 * stage);
+                            tma_load_2d(b_dst, tb, kb * BK, n_cta, bFULL + 8 * stage);
                         } else {
                             // the leader arms its barrier for the bytes of both CTAs
-                            if (rank == 0) mbar_arrive_expect_tx(bFULL + 8 * stage, 2 * SLOT_BYTES);
+                            if (rank == 0) mbar_arrive_expect_tx(bFULL + 8 * stage, 2 * bytes);
                             tma_load_2d_pair(a_dst, &tmA, kb * BK, m_cta, full_leader + 8 * stage);
-                            tma_load_2d_pair(b_dst, &tmB, kb * BK, n_cta, full_leader + 8 * stage);
+                            tma_load_2d_pair(b_dst, tb, kb * BK, n_cta, full_leader + 8 * stage);
                         }
                         ++issued;
                         if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -420,14 +447,17 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (is_leader && lane == 0) {
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleMma};
             constexpr uint32_t IDESC = make_idesc<SH::UMMA_M, SH::UMMA_N>();
+            constexpr uint32_t IDESC_HALF = make_idesc<SH::UMMA_M, SH::UMMA_N / 2>();   // half-width units
             uint32_t stage = 0, phase = 0;
             uint32_t tcount = 0;
             bool ok = true, issued_any = false;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++tcount) {
+            for (int u = cluster_id; ok && u < p.total_units; u += num_clusters, ++tcount) {
+                const Unit un = unit_of(u, p);
                 const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
                 if (!W.template wait<CG == 2>(bTEMPTY + 8 * b, aph)) { ok = false; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * SH::ACC_COLS;
+                const uint32_t idesc = un.half >= 0 ? IDESC_HALF : IDESC;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!W.wait(bFULL + 8 * stage, phase)) { ok = false; break; }
                     tc_fence_after_sync();
@@ -437,7 +467,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         // +32 bytes of K per step: +2 in the (address >> 4) field
-                        tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+                        tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
                     }
                     issued_any = true;
                     // release the slot once these multiplies have read it
@@ -473,8 +503,48 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 else mbar_arrive_cluster(tempty_leader + 8 * b);
             }
         }
-        uint32_t tcount = 0, sbuf = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++tcount) {
+        uint32_t sbuf = 0;
+        // Writes 64 f16 columns (h: 32 packed pairs) of this lane's row of a
+        // 32-row block: through swizzled staging and a TMA store (clipped at M
+        // and N), or with guarded plain stores.
+        auto store_chunk = [&](const uint32_t(&h)[32], int row0, int col0) {
+            if (p.store == kStoreTma) {
+                const uint32_t buf = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF + sbuf * EPI_BUF;
+                // the store issued from this buffer two chunks ago has finished reading it
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h[4 * j]),
+                                 "r"(h[4 * j + 1]), "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                // a box wholly past M or N (padding rows of a pair tile) is not stored
+                if (lane == 0 && row0 < p.M && col0 < p.N) {
+                    tma_store_2d(&tmC, buf, col0, row0);
+                    bulk_commit_group();
+                }
+                sbuf ^= 1u;
+            } else {
+                const int row = row0 + lane;
+                if (row < p.M) {
+                    unsigned short* dst = reinterpret_cast<unsigned short*>(p.out) + static_cast<int64_t>(row) * p.N;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = col0 + 2 * i;
+                        if (col < p.N) dst[col] = static_cast<unsigned short>(h[i] & 0xFFFFu);
+                        if (col + 1 < p.N) dst[col + 1] = static_cast<unsigned short>(h[i] >> 16);
+                    }
+                }
+            }
+        };
+        uint32_t tcount = 0;
+        for (int u = cluster_id; u < p.total_units; u += num_clusters, ++tcount) {
+            const Unit un = unit_of(u, p);
             const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
             bool got = true;
             if (lane == 0) got = W.wait(bTFULL + 8 * b, aph);
@@ -482,9 +552,13 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             if (!got) break;
             tc_fence_after_sync();
             int tm, tn;
-            tile_coords(t, p, tm, tn);
+            tile_coords(un.tile, p, tm, tn);
             const int row0 = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA + q * 32;
-            for (int c = 0; c < SH::ACC_COLS / EPI_COLS; ++c) {
+            // a half-width unit holds UMMA_N / 2 accumulator columns, starting
+            // at column half * UMMA_N / 2 of its tile
+            const int ncols = un.half >= 0 ? SH::ACC_COLS / 2 : SH::ACC_COLS;
+            const int col_base = tn * SH::UMMA_N + (un.half > 0 ? SH::UMMA_N / 2 : 0);
+            for (int c = 0; c < ncols / EPI_COLS; ++c) {
                 uint32_t v0[32], v1[32];
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * SH::ACC_COLS +
                                        static_cast<uint32_t>(c * EPI_COLS);
@@ -496,40 +570,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 for (int i = 0; i < 16; ++i) h[i] = pack_half2(v0[2 * i], v0[2 * i + 1]);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) h[16 + i] = pack_half2(v1[2 * i], v1[2 * i + 1]);
-                const int col0 = tn * SH::UMMA_N + c * EPI_COLS;
-                if (p.store == kStoreTma) {
-                    const uint32_t buf = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF + sbuf * EPI_BUF;
-                    // the store issued from this buffer two chunks ago has finished reading it
-                    if (lane == 0) bulk_wait_group_read<1>();
-                    __syncwarp();
-                    const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h[4 * j]),
-                                     "r"(h[4 * j + 1]), "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
-                                     : "memory");
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    // a box wholly past M or N (padding rows of a pair tile) is not stored
-                    if (lane == 0 && row0 < p.M && col0 < p.N) {
-                        tma_store_2d(&tmC, buf, col0, row0);
-                        bulk_commit_group();
-                    }
-                    sbuf ^= 1u;
-                } else {
-                    const int row = row0 + lane;
-                    if (row < p.M) {
-                        unsigned short* dst = reinterpret_cast<unsigned short*>(p.out) + static_cast<int64_t>(row) * p.N;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int col = col0 + 2 * i;
-                            if (col < p.N) dst[col] = static_cast<unsigned short>(h[i] & 0xFFFFu);
-                            if (col + 1 < p.N) dst[col + 1] = static_cast<unsigned short>(h[i] >> 16);
-                        }
-                    }
-                }
+                store_chunk(h, row0, col_base + c * EPI_COLS);
             }
             // this warp's reads of accumulator buffer b are complete
             tc_fence_before_sync();
@@ -687,26 +728,76 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     return pl;
 }
 
+inline int block_threads(const Plan& pl) {
+    return ((pl.producer == kProducerTma ? 1 : COPY_WARPS) + 1 + EPI_WARPS) * 32;
+}
+
+// Sets the kernel's shared-memory limit (once per device) and returns how
+// many CTA groups (pairs or single CTAs) can be resident at once: the size of
+// the persistent grid.  0 on failure.
 template <int CG, int S>
-int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-           const Params& p, cudaStream_t stream) {
+int capacity(const DeviceInfo& info, int threads) {
     auto kern = gemm_f16_nt_kernel<CG, S>;
     constexpr int smem = Layout<S>::DYN;
     static_assert(Layout<S>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
     static int configured[64] = {};
     static int max_clusters[64] = {};
-    const int threads = ((pl.producer == kProducerTma ? 1 : COPY_WARPS) + 1 + EPI_WARPS) * 32;
     if (!configured[info.device]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return GEMM_ERR_LAUNCH;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
         configured[info.device] = 1;
     }
+    if constexpr (CG == 1) {
+        return info.num_sms;
+    } else {
+        if (!max_clusters[info.device]) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            cfg.blockDim = dim3(threads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cfg.gridDim = dim3(2 * info.num_sms, 1, 1);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = info.num_sms / 2;
+            }
+            max_clusters[info.device] = n;
+        }
+        return max_clusters[info.device];
+    }
+}
+
+template <int CG>
+int capacity_for(int stages, const DeviceInfo& info, int threads) {
+    switch (stages) {
+        case 1: return capacity<CG, 1>(info, threads);
+        case 2: return capacity<CG, 2>(info, threads);
+        case 3: return capacity<CG, 3>(info, threads);
+        case 4: return capacity<CG, 4>(info, threads);
+        case 5: return capacity<CG, 5>(info, threads);
+        default: return capacity<CG, 6>(info, threads);
+    }
+}
+
+// Launches the persistent grid: one CTA group per work unit, at most as many
+// as can be resident.
+template <int CG, int S>
+int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
+           const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
+    auto kern = gemm_f16_nt_kernel<CG, S>;
+    const int threads = block_threads(pl);
+    const int cap = capacity<CG, S>(info, threads);
+    if (cap <= 0) return GEMM_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = Layout<S>::DYN;
     cfg.stream = stream;
-    int grid_ctas;
     if constexpr (CG == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
@@ -714,37 +805,26 @@ int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const 
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (!max_clusters[info.device]) {
-            int n = 0;
-            cfg.gridDim = dim3(2 * info.num_sms, 1, 1);
-            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-                cudaGetLastError();
-                n = info.num_sms / 2;
-            }
-            max_clusters[info.device] = n;
-        }
-        const int clusters = pl.num_tiles < max_clusters[info.device] ? pl.num_tiles : max_clusters[info.device];
-        grid_ctas = 2 * clusters;
     } else {
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
-        grid_ctas = pl.num_tiles < info.num_sms ? pl.num_tiles : info.num_sms;
     }
-    cfg.gridDim = dim3(grid_ctas, 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    const int groups = p.total_units < cap ? p.total_units : cap;
+    cfg.gridDim = dim3(CG * groups, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tc, p) != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
 template <int CG>
 int launch_stages(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
-                  const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
+                  const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
     switch (stages) {
-        case 1: return launch<CG, 1>(pl, info, ta, tb, tc, p, stream);
-        case 2: return launch<CG, 2>(pl, info, ta, tb, tc, p, stream);
-        case 3: return launch<CG, 3>(pl, info, ta, tb, tc, p, stream);
-        case 4: return launch<CG, 4>(pl, info, ta, tb, tc, p, stream);
-        case 5: return launch<CG, 5>(pl, info, ta, tb, tc, p, stream);
-        case 6: return launch<CG, 6>(pl, info, ta, tb, tc, p, stream);
+        case 1: return launch<CG, 1>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 2: return launch<CG, 2>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 3: return launch<CG, 3>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 4: return launch<CG, 4>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 5: return launch<CG, 5>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 6: return launch<CG, 6>(pl, info, ta, tb, tbh, tc, p, stream);
         default: return GEMM_ERR_UNSUPPORTED_STAGES;
     }
 }
@@ -858,8 +938,32 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     p.rhs = reinterpret_cast<const __half*>(rhs);
     p.out = reinterpret_cast<__half*>(out);
     p.status = info.status;
-    if (pl.cg == 2) return done(launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream));
-    return done(launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream));
+    p.full_units = pl.num_tiles;
+    p.split = 0;
+    p.total_units = pl.num_tiles;
+
+    // Tail split: when the tiles leave a last, partial wave of the persistent
+    // grid (or fewer tiles than the grid) and twice that many units still
+    // fit in one wave, each of those tiles runs as two half-width units on the
+    // wave's otherwise idle CTA groups.  Only the TMA producer supports it (it
+    // needs the 64-row B box).  Each output element is still one in-order K
+    // sum; the decision depends on the shape and the device, never on S.
+    CUtensorMap tbh;
+    memset(&tbh, 0, sizeof(tbh));
+    const int cap = pl.cg == 2 ? capacity_for<2>(stages, info, block_threads(pl))
+                               : capacity_for<1>(stages, info, block_threads(pl));
+    if (cap <= 0) return done(GEMM_ERR_LAUNCH);
+    const int waves = pl.num_tiles / cap;
+    const int tail = pl.num_tiles - waves * cap;
+    if (pl.producer == kProducerTma && tail > 0 && 2 * tail <= cap && !(flags & GEMM_DEBUG_NO_SPLIT)) {
+        if (!encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return done(GEMM_ERR_LAUNCH);
+        p.full_units = waves * cap;
+        p.split = 2;
+        p.total_units = waves * cap + 2 * tail;
+    }
+    const int rc2 = pl.cg == 2 ? launch_stages<2>(stages, pl, info, ta, tb, tbh, tc, p, stream)
+                               : launch_stages<1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    return done(rc2);
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -980,6 +1084,11 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     p.rhs = reinterpret_cast<const __half*>(rhs);
     p.out = reinterpret_cast<__half*>(out);
     p.status = info.status;
-    if (pl.cg == 2) return launch_stages<2>(stages, pl, info, ta, tb, tc, p, stream);
-    return launch_stages<1>(stages, pl, info, ta, tb, tc, p, stream);
+    p.full_units = pl.num_tiles;        // whole tiles only
+    p.split = 0;
+    p.total_units = pl.num_tiles;
+    CUtensorMap tbh;                    // unused without the tail split
+    memset(&tbh, 0, sizeof(tbh));
+    if (pl.cg == 2) return launch_stages<2>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    return launch_stages<1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
 }

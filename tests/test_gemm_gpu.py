@@ -180,6 +180,23 @@ def test_f16_edge_shapes(M, N, K, flags):
         assert_f16_ok(run_f16(a, b, s, flags), oracle.gemm_f16_nt_f64(a, b), K)
 
 
+@pytest.mark.parametrize("M,N,K,flags", [
+    (1024, 1024, 1024, 0),                                # 64 single tiles < 152 SMs: every tile split in 2
+    (700, 650, 1000, pws.GEMM_DEBUG_FORCE_PAIR_TILE),     # 9 pair tiles: split in 4 (>= 4 K blocks each)
+    (2300, 2100, 768, 0),                                 # 9 x 9 pair tiles = 81 > 76: a 5-tile tail split
+])
+def test_f16_tail_split_matches_unsplit(M, N, K, flags):
+    a = inputs.uniform_f16(M + N, 0, (M, K))
+    b = inputs.uniform_f16(M + N, 1, (N, K))
+    ref = oracle.gemm_f16_nt_f64(a, b)
+    split = run_f16(a, b, 3, flags)
+    whole = run_f16(a, b, 3, flags | pws.GEMM_DEBUG_NO_SPLIT)
+    assert_f16_ok(split, ref, K)
+    assert_f16_ok(whole, ref, K)
+    # the split changes only the fp32 summation order: the two agree under the same rule
+    assert_f16_ok(split, whole.astype(np.float64), K)
+
+
 def test_f16_k_zero_and_empty():
     a = np.zeros((7, 0), np.float16)
     b = np.zeros((5, 0), np.float16)
