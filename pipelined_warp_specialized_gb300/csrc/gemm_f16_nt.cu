@@ -274,15 +274,17 @@ __device__ __forceinline__ void copy_strip(uint32_t slot, const __half* base, in
 }
 
 // The producer loop of the copy path.  Each thread's copies of K block k form
-// one cp.async group; the slot of block k is signalled LAG = S - 1 blocks
-// later, once the thread's groups up to k have landed (cp.async.wait_group),
-// after a proxy fence (the tensor core reads through the async proxy) and a
-// warp barrier, by one arrive per warp.  LAG <= S - 1 keeps the ring live:
-// the wait on empty for block k needs full for block k - S already signalled.
+// one cp.async group; the slot of block k is signalled LAG blocks later, once
+// the thread's groups up to k have landed (cp.async.wait_group), after a proxy
+// fence (the tensor core reads through the async proxy) and a warp barrier,
+// by one arrive per warp.  The MMA thread takes GROUP slots at a time (2 when
+// S = 6), so LAG = S - GROUP keeps the ring live: the wait on empty for block
+// k needs block k - S consumed, which needs full signalled up to block
+// k - S + GROUP - 1.
 template <int G, int S>
 __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB, uint32_t bFULL,
                               uint32_t bEMPTY, int cluster_id, int num_clusters, int lane) {
-    constexpr int LAG = S - 1;
+    constexpr int LAG = S - (S >= 6 ? 2 : 1);
     const int t = threadIdx.x;                   // 0 .. COPY_THREADS - 1
     uint32_t stage = 0, phase = 0, issued = 0, signalled = 0;
     bool ok = true;
@@ -458,22 +460,44 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * SH::ACC_COLS;
                 const uint32_t idesc = un.half >= 0 ? IDESC_HALF : IDESC;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!W.wait(bFULL + 8 * stage, phase)) { ok = false; break; }
+                // With S = 6 the MMA thread takes the ring's slots two at a time:
+                // it waits for both, issues their 8 MMAs back to back and then
+                // commits both.  A wait/commit boundary after every 4 MMAs
+                // measurably idles the tensor pipe (about 2 % sustained at
+                // 8192^3).  Holding two slots leaves the producer S - 2 to fill
+                // ahead, which only the 6-slot ring can afford: measured on
+                // GB300, pairing is 11 % slower at S = 4 and 2 % slower at S = 5.
+                constexpr int GROUP = S >= 6 ? 2 : 1;
+                for (int kb = 0; kb < p.num_kb; kb += GROUP) {
+                    const int nb = p.num_kb - kb < GROUP ? p.num_kb - kb : GROUP;
+                    uint32_t st[GROUP], ph[GROUP];
+                    st[0] = stage;
+                    ph[0] = phase;
+                    if constexpr (GROUP == 2) {
+                        st[1] = stage + 1 == S ? 0u : stage + 1;
+                        ph[1] = stage + 1 == S ? phase ^ 1u : phase;
+                    }
+                    for (int j = 0; j < nb; ++j)
+                        if (!W.wait(bFULL + 8 * st[j], ph[j])) { ok = false; break; }
+                    if (!ok) break;
                     tc_fence_after_sync();
                     if (p.producer == kProducerCopy) fence_proxy_async_smem();
-                    const uint64_t adesc = make_sdesc(sA + stage * A_SLOT);
-                    const uint64_t bdesc = make_sdesc(sB + stage * B_SLOT);
+                    for (int j = 0; j < nb; ++j) {
+                        const uint64_t adesc = make_sdesc(sA + st[j] * A_SLOT);
+                        const uint64_t bdesc = make_sdesc(sB + st[j] * B_SLOT);
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
-                        // +32 bytes of K per step: +2 in the (address >> 4) field
-                        tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            // +32 bytes of K per step: +2 in the (address >> 4) field
+                            tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j) != 0 || k != 0);
+                        }
                     }
                     issued_any = true;
-                    // release the slot once these multiplies have read it
-                    if constexpr (CG == 1) tc_commit_1(bEMPTY + 8 * stage);
-                    else tc_commit_2_mc(bEMPTY + 8 * stage, 0x3);
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    // release the slots once these multiplies have read them
+                    for (int j = 0; j < nb; ++j) {
+                        if constexpr (CG == 1) tc_commit_1(bEMPTY + 8 * st[j]);
+                        else tc_commit_2_mc(bEMPTY + 8 * st[j], 0x3);
+                        if (++stage == S) { stage = 0; phase ^= 1u; }
+                    }
                 }
                 if (!ok) break;
                 // accumulator of this tile is complete
