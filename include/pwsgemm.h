@@ -128,12 +128,11 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  *
  * The kernel is persistent: a grid of as many CTA groups as fit on the GPU
  * strides over the output tiles.  When the tile count leaves a last, partial
- * wave, each tile of that wave is cut along K into parts that run on the
- * wave's otherwise idle CTA groups; the parts' fp32 partial sums go to
- * scratch from the same pool, and the last part to finish adds them in part
- * order before rounding to f16 (so the result depends on the shape and the
- * device's SM count, not on S or on timing).  If the pool cannot supply that
- * scratch the tiles are not cut.
+ * wave that fills at most half of the grid, each tile of that wave runs as
+ * two units, its left and right halves of columns, on the wave's otherwise
+ * idle CTA groups.  Each half runs the whole K loop, so no partial sums are
+ * combined, no scratch is needed and every output element has the same
+ * summation order whether or not its tile was split.
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT (a pointer not
  * 2-byte aligned), GEMM_ERR_UNSUPPORTED_STAGES, GEMM_ERR_UNSUPPORTED_ARCH or
