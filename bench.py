@@ -86,9 +86,10 @@ def kernel_sha() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(M, N, K):
-    """DRAM bytes per launch from the committed ncu summary, scaled to this
-    shape, or None if absent or taken on another version of the kernel."""
+def profiled_traffic(M, N, K, S):
+    """DRAM bytes per launch from the committed ncu summary of this shape and
+    stage count, or None if absent, taken on another shape or S (S selects the
+    tile) or on another version of the kernel."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     vals = {}
@@ -100,7 +101,7 @@ def profiled_traffic(M, N, K):
     try:
         if vals.get("kernel_sha") != kernel_sha():
             return None
-        if (int(vals["M"]), int(vals["N"]), int(vals["K"])) != (M, N, K):
+        if (int(vals["M"]), int(vals["N"]), int(vals["K"]), int(vals["stages"])) != (M, N, K, S):
             return None
         return float(vals["dram_bytes_per_launch"])
     except (KeyError, ValueError):
@@ -306,8 +307,10 @@ def extra_configs(pws, torch, stream, reps=20):
                     else:
                         ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3,
                                            torch, stream)
+                    ps = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), s)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
-                                    "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1)}
+                                    "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1),
+                                    "tile": f"{ps['bm']}x{ps['bn']}"}
                     if small and not plan["producer"] == 2:
                         res[f"S{s}"]["timing"] = "CUDA-graph replay"
             finally:
@@ -390,12 +393,15 @@ def run_ours(args, world, rank, local):
     long_region = ms_total > 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     achieved = flops / ms / 1e9
-    roofline = {"bound": "tensor", "kernel": "gemm_f16_nt_kernel<2,S>" if M * N >= 2 ** 20 else "gemm_f16_nt_kernel",
+    plan = pws.gemm_f16_nt_plan(M, N, K, stages=S)
+    nw = plan["bn"] // (128 * plan["cta_group"])
+    roofline = {"bound": "tensor", "kernel": f"gemm_f16_nt_kernel<{plan['cta_group']},{S},{nw}>",
+                "tile": f"{plan['bm']}x{plan['bn']}",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
                 "peak_source": f"{peak_src} {'sustained' if long_region else 'burst'} dense bf16 "
                                "(f16 and bf16 share the tensor rate)",
-                "traffic": profiled_traffic(M, N, K),
+                "traffic": profiled_traffic(M, N, K, S),
                 "algorithmic_bytes_per_launch": int((M * K + N * K + M * N) * 2)}
 
     extras = None
@@ -492,8 +498,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--stages", type=int, default=6,
-                    help="ring slots S of the timed GEMM (6: the fastest sustained configuration on GB300)")
+    ap.add_argument("--stages", type=int, default=4,
+                    help="ring slots S of the timed GEMM (4: the wide 256x512 pair tile, the fastest "
+                         "sustained configuration on GB300; 5 and 6 run the 256x256 tile)")
     ap.add_argument("--workload", default="f16_nt_8192", choices=[k for k in inputs.WORKLOADS if k.startswith("f16")],
                     help="the seeded f16 workload of the timed GEMM")
     ap.add_argument("--shape", default=None, help="M,N,K override (uniform [-1,1) inputs, seed 5)")

@@ -126,6 +126,15 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  * operands instead.  Partial tiles are zero-filled on load and clipped on
  * store.
  *
+ * Output tiles: 256 x 256 on a CTA pair (two SMs sharing one tcgen05 MMA),
+ * or 128 x 128 on one CTA for outputs too small to occupy the GPU with pairs
+ * and for the asynchronous-copy producer.  With stages <= 4 the pair uses a
+ * 256 x 512 tile instead where that adds no padding columns: each ring slot
+ * then carries two B boxes, so each operand byte copied into shared memory
+ * feeds 4/3 as many flops (5 and 6 slots of that size do not fit in shared
+ * memory).  Every tile sums each output element over K in the same order,
+ * so the tile choice never changes the result.
+ *
  * The kernel is persistent: a grid of as many CTA groups as fit on the GPU
  * strides over the output tiles.  When the tile count leaves a last, partial
  * wave that fills at most half of the grid, each tile of that wave runs as
@@ -206,8 +215,12 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *       the CTA-pair 256x256 tile would be chosen.
  *   GEMM_DEBUG_FORCE_PAIR_TILE     : use the CTA-pair 256x256 tile whenever the
  *       TMA producer is used, even for small outputs.
- *   GEMM_DEBUG_NO_SPLIT            : do not split the last wave's tiles along K
- *       (gemm_f16_nt normally does, see below).
+ *   GEMM_DEBUG_NO_SPLIT            : do not split the last wave's tiles into
+ *       half-width units (gemm_f16_nt normally does, see above).
+ *   GEMM_DEBUG_FORCE_NARROW_TILE   : where the CTA pair is used, always use
+ *       its 256x256 tile, never the wide 256x512 one.
+ *   GEMM_DEBUG_FORCE_WIDE_TILE     : where the CTA pair is used and stages is
+ *       at most 4, always use the wide 256x512 tile.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -216,7 +229,9 @@ enum {
     GEMM_DEBUG_FORCE_DIRECT_STORE = 4u,
     GEMM_DEBUG_FORCE_SOLO_TILE = 8u,
     GEMM_DEBUG_FORCE_PAIR_TILE = 16u,
-    GEMM_DEBUG_NO_SPLIT = 32u
+    GEMM_DEBUG_NO_SPLIT = 32u,
+    GEMM_DEBUG_FORCE_NARROW_TILE = 64u,
+    GEMM_DEBUG_FORCE_WIDE_TILE = 128u
 };
 int gemm_set_debug_flags(unsigned flags);
 

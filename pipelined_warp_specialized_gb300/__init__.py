@@ -35,6 +35,8 @@ GEMM_DEBUG_FORCE_DIRECT_STORE = 4
 GEMM_DEBUG_FORCE_SOLO_TILE = 8
 GEMM_DEBUG_FORCE_PAIR_TILE = 16
 GEMM_DEBUG_NO_SPLIT = 32
+GEMM_DEBUG_FORCE_NARROW_TILE = 64
+GEMM_DEBUG_FORCE_WIDE_TILE = 128
 
 _lib = None
 

@@ -109,20 +109,31 @@ struct Params {
     int total_units;
 };
 
-template <int CG>
+// NW = MMAs per K step, each UMMA_N columns wide.  NW = 1: the accumulator is
+// double buffered.  NW = 2 (CTA pair only, "wide" 256 x 512 tile): one
+// accumulator fills all 512 tensor-memory columns and each slot carries two B
+// boxes, so every byte copied into shared memory feeds 4/3 as many flops.
+template <int CG, int NW = 1>
 struct Shape {
     static constexpr int UMMA_M = BM_CTA * CG;        // tile rows (per CTA group)
-    static constexpr int UMMA_N = BN_CTA * CG;        // tile columns
-    static constexpr int ACC_COLS = UMMA_N;           // fp32 columns per accumulator
-    static constexpr int TMEM_COLS = 2 * ACC_COLS;    // double-buffered accumulator
+    static constexpr int UMMA_N = BN_CTA * CG;        // columns per MMA
+    static constexpr int TILE_N = UMMA_N * NW;        // tile columns
+    static constexpr int ACC_COLS = TILE_N;           // fp32 columns per accumulator
+    static constexpr int NBUF = NW == 1 ? 2 : 1;      // accumulator buffers
+    static constexpr int TMEM_COLS = NBUF * ACC_COLS;
+    // a split (half-width) unit covers HALF_N columns of its tile
+    static constexpr int HALF_N = NW == 1 ? UMMA_N / 2 : UMMA_N;
+    static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
 
-// Shared-memory carve-up (offsets from a 1024-byte aligned base).
-template <int S>
+// Shared-memory carve-up (offsets from a 1024-byte aligned base).  Slot s
+// holds A at A + s * A_SLOT and its NW B boxes at B + s * NW * B_SLOT.
+template <int S, int NW = 1>
 struct Layout {
+    static constexpr int B_STRIDE = NW * B_SLOT;
     static constexpr int A = 0;
     static constexpr int B = S * A_SLOT;
-    static constexpr int EPI = S * SLOT_BYTES;
+    static constexpr int EPI = S * (A_SLOT + B_STRIDE);
     static constexpr int BAR = EPI + EPI_BYTES;
     static constexpr int FULL = BAR;
     static constexpr int EMPTY = FULL + 8 * S;
@@ -320,13 +331,16 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
     }
 }
 
-template <int CG, int S>
-__global__ void __launch_bounds__((COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
+// A CTA pair is always fed by TMA (one producer warp): its bound lets the
+// compiler use the registers the cp.async producer's eight warps would need.
+template <int CG, int S, int NW>
+__global__ void __launch_bounds__((CG == 2 ? 1 + 1 + EPI_WARPS : COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ Params p) {
-    using SH = Shape<CG>;
-    using L = Layout<S>;
+    static_assert(NW == 1 || CG == 2, "the wide tile is a CTA-pair tile");
+    using SH = Shape<CG, NW>;
+    using L = Layout<S, NW>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     const uint32_t raw = smem_u32(smem_raw);
@@ -395,15 +409,19 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     int tm, tn;
                     tile_coords(un.tile, p, tm, tn);
                     const int m_cta = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA;
-                    // a half-width unit loads half of the CTA's B rows (tmBh: a 64-row box)
                     const bool halfw = un.half >= 0;
-                    const int n_cta = halfw ? tn * SH::UMMA_N + un.half * (SH::UMMA_N / 2) + static_cast<int>(rank) * (BN_CTA / 2)
-                                            : tn * SH::UMMA_N + static_cast<int>(rank) * BN_CTA;
-                    const CUtensorMap* tb = halfw ? &tmBh : &tmB;
-                    const uint32_t bytes = halfw ? A_SLOT + B_SLOT / 2 : SLOT_BYTES;
+                    // NW = 1: a half-width unit loads half of the CTA's B rows
+                    // (tmBh: a 64-row box).  NW = 2: box h of the CTA's B rows
+                    // starts at column h * UMMA_N of the unit; a half-width unit
+                    // is one such box.
+                    const int n_unit = tn * SH::TILE_N + (halfw ? un.half * SH::HALF_N : 0);
+                    const int n_cta = n_unit + static_cast<int>(rank) * (NW == 1 && halfw ? BN_CTA / 2 : BN_CTA);
+                    const CUtensorMap* tb = NW == 1 && halfw ? &tmBh : &tmB;
+                    const int nbox = NW == 1 || halfw ? 1 : NW;
+                    const uint32_t bytes = NW == 1 && halfw ? A_SLOT + B_SLOT / 2 : A_SLOT + nbox * B_SLOT;
                     for (int kb = 0; kb < p.num_kb; ++kb) {
                         if (!W.wait(bEMPTY + 8 * stage, phase)) { ok = false; break; }
-                        const uint32_t a_dst = sA + stage * A_SLOT, b_dst = sB + stage * B_SLOT;
+                        const uint32_t a_dst = sA + stage * A_SLOT, b_dst = sB + stage * L::B_STRIDE;
                         if constexpr (CG == 1) {
                             mbar_arrive_expect_tx(bFULL + 8 * stage, bytes);
                             tma_load_2d(a_dst, &tmA, kb * BK, m_cta, bFULL + 8 * stage);
@@ -412,7 +430,9 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                             // the leader arms its barrier for the bytes of both CTAs
                             if (rank == 0) mbar_arrive_expect_tx(bFULL + 8 * stage, 2 * bytes);
                             tma_load_2d_pair(a_dst, &tmA, kb * BK, m_cta, full_leader + 8 * stage);
-                            tma_load_2d_pair(b_dst, tb, kb * BK, n_cta, full_leader + 8 * stage);
+                            for (int h = 0; h < nbox; ++h)
+                                tma_load_2d_pair(b_dst + h * B_SLOT, tb, kb * BK, n_cta + h * SH::UMMA_N,
+                                                 full_leader + 8 * stage);
                         }
                         ++issued;
                         if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -448,61 +468,189 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         if (is_leader && lane == 0) {
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleMma};
-            constexpr uint32_t IDESC = make_idesc<SH::UMMA_M, SH::UMMA_N>();
-            constexpr uint32_t IDESC_HALF = make_idesc<SH::UMMA_M, SH::UMMA_N / 2>();   // half-width units
             uint32_t stage = 0, phase = 0;
-            uint32_t tcount = 0;
             bool ok = true, issued_any = false;
-            for (int u = cluster_id; ok && u < p.total_units; u += num_clusters, ++tcount) {
-                const Unit un = unit_of(u, p);
-                const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
-                if (!W.template wait<CG == 2>(bTEMPTY + 8 * b, aph)) { ok = false; break; }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * SH::ACC_COLS;
-                const uint32_t idesc = un.half >= 0 ? IDESC_HALF : IDESC;
-                // With S = 6 the MMA thread takes the ring's slots two at a time:
-                // it waits for both, issues their 8 MMAs back to back and then
-                // commits both.  A wait/commit boundary after every 4 MMAs
-                // measurably idles the tensor pipe (about 2 % sustained at
-                // 8192^3).  Holding two slots leaves the producer S - 2 to fill
-                // ahead, which only the 6-slot ring can afford: measured on
-                // GB300, pairing is 11 % slower at S = 4 and 2 % slower at S = 5.
-                constexpr int GROUP = S >= 6 ? 2 : 1;
-                for (int kb = 0; kb < p.num_kb; kb += GROUP) {
-                    const int nb = p.num_kb - kb < GROUP ? p.num_kb - kb : GROUP;
-                    uint32_t st[GROUP], ph[GROUP];
-                    st[0] = stage;
-                    ph[0] = phase;
-                    if constexpr (GROUP == 2) {
-                        st[1] = stage + 1 == S ? 0u : stage + 1;
-                        ph[1] = stage + 1 == S ? phase ^ 1u : phase;
-                    }
-                    for (int j = 0; j < nb; ++j)
-                        if (!W.wait(bFULL + 8 * st[j], ph[j])) { ok = false; break; }
-                    if (!ok) break;
+            if constexpr (NW == 1) {
+                constexpr uint32_t IDESC = make_idesc<SH::UMMA_M, SH::UMMA_N>();
+                constexpr uint32_t IDESC_HALF = make_idesc<SH::UMMA_M, SH::UMMA_N / 2>();   // half-width units
+                uint32_t tcount = 0;
+                for (int u = cluster_id; ok && u < p.total_units; u += num_clusters, ++tcount) {
+                    const Unit un = unit_of(u, p);
+                    const uint32_t b = tcount % SH::NBUF, aph = (tcount / SH::NBUF) & 1u;
+                    if (!W.template wait<CG == 2>(bTEMPTY + 8 * b, aph)) { ok = false; break; }
                     tc_fence_after_sync();
-                    if (p.producer == kProducerCopy) fence_proxy_async_smem();
-                    for (int j = 0; j < nb; ++j) {
-                        const uint64_t adesc = make_sdesc(sA + st[j] * A_SLOT);
-                        const uint64_t bdesc = make_sdesc(sB + st[j] * B_SLOT);
+                    const uint32_t d_tmem = tmem_base + b * SH::ACC_COLS;
+                    // a half-width unit is one MMA of N = UMMA_N / 2
+                    const uint32_t idesc = un.half >= 0 ? IDESC_HALF : IDESC;
+                    // With S = 6 the MMA thread takes the ring's slots two at a time:
+                    // it waits for both, issues their 8 MMAs back to back and then
+                    // commits both.  A wait/commit boundary after every 4 MMAs
+                    // measurably idles the tensor pipe (about 2 % sustained at
+                    // 8192^3).  Holding two slots leaves the producer S - 2 to fill
+                    // ahead, which only the 6-slot ring can afford: measured on
+                    // GB300, pairing is 11 % slower at S = 4 and 2 % slower at S = 5.
+                    constexpr int GROUP = S >= 6 ? 2 : 1;
+                    for (int kb = 0; kb < p.num_kb; kb += GROUP) {
+                        const int nb = p.num_kb - kb < GROUP ? p.num_kb - kb : GROUP;
+                        uint32_t st[GROUP], ph[GROUP];
+                        st[0] = stage;
+                        ph[0] = phase;
+                        if constexpr (GROUP == 2) {
+                            st[1] = stage + 1 == S ? 0u : stage + 1;
+                            ph[1] = stage + 1 == S ? phase ^ 1u : phase;
+                        }
+                        for (int j = 0; j < nb; ++j)
+                            if (!W.wait(bFULL + 8 * st[j], ph[j])) { ok = false; break; }
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        if (p.producer == kProducerCopy) fence_proxy_async_smem();
+                        for (int j = 0; j < nb; ++j) {
+                            const uint64_t adesc = make_sdesc(sA + st[j] * A_SLOT);
+                            const uint64_t bdesc = make_sdesc(sB + st[j] * B_SLOT);
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            // +32 bytes of K per step: +2 in the (address >> 4) field
-                            tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j) != 0 || k != 0);
+                            for (int k = 0; k < BK / UMMA_K; ++k) {
+                                // +32 bytes of K per step: +2 in the (address >> 4) field
+                                tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j) != 0 || k != 0);
+                            }
+                        }
+                        issued_any = true;
+                        // release the slots once these multiplies have read them
+                        for (int j = 0; j < nb; ++j) {
+                            if constexpr (CG == 1) tc_commit_1(bEMPTY + 8 * st[j]);
+                            else tc_commit_2_mc(bEMPTY + 8 * st[j], 0x3);
+                            if (++stage == S) { stage = 0; phase ^= 1u; }
                         }
                     }
-                    issued_any = true;
-                    // release the slots once these multiplies have read them
-                    for (int j = 0; j < nb; ++j) {
-                        if constexpr (CG == 1) tc_commit_1(bEMPTY + 8 * st[j]);
-                        else tc_commit_2_mc(bEMPTY + 8 * st[j], 0x3);
-                        if (++stage == S) { stage = 0; phase ^= 1u; }
+                    if (!ok) break;
+                    // accumulator of this tile is complete
+                    if constexpr (CG == 1) tc_commit_1(bTFULL + 8 * b);
+                    else tc_commit_2_mc(bTFULL + 8 * b, 0x3);
+                }
+            } else {
+                // The wide tile's accumulator is one buffer, drained in two
+                // halves of UMMA_N columns with an event pair each (tmem_full[h]
+                // / tmem_empty[h]).  At both ends of a unit the K blocks of a
+                // group of J run half 0 and then half 1 on the same, still held,
+                // slots: the epilogue drains half 0 of unit i while the tensor
+                // pipe finishes half 1, and half 1 while half 0 of unit i+1
+                // starts, so the pipe does not wait for the whole accumulator.
+                // J = S - 1 leaves the producer one slot to fill while a group
+                // is held.  A half-width unit uses half 0 only.
+                //
+                // The issuing thread's own instructions between MMAs idle the
+                // tensor pipe (measured on GB300: the same MMAs issued from a
+                // general loop over groups, halves and blocks ran 30-50 %
+                // slower), so each part of a unit is straight-line code with
+                // compile-time trip counts, and the descriptors of slot s are
+                // the slot-0 descriptors plus s times the slot size: the start
+                // address field (bits 0..13, address >> 4) cannot carry, as all
+                // of shared memory lies below 256 KB.
+                constexpr uint32_t IDESC = make_idesc<SH::UMMA_M, SH::UMMA_N>();
+                constexpr int J = S > 1 ? S - 1 : 1;
+                const uint64_t adesc0 = make_sdesc(sA), bdesc0 = make_sdesc(sB);
+                uint32_t used0 = 0u, used1 = 0u;   // units that have used half 0 / half 1 so far
+                const int nkb = p.num_kb;
+                auto slot = [](uint32_t x) { return x < static_cast<uint32_t>(S) ? x : x - S; };
+                // the 4 MMAs of the K block in slot s for half h (`first`: the unit's first K block)
+                auto mma_block = [&](uint32_t s, int h, bool first) {
+                    const uint64_t a = adesc0 + s * (A_SLOT >> 4);
+                    const uint64_t b = bdesc0 + s * (L::B_STRIDE >> 4) + h * (B_SLOT >> 4);
+                    const uint32_t d = tmem_base + h * SH::UMMA_N;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        tc_mma_f16<CG>(d, a + 2 * k, b + 2 * k, IDESC, !(first && k == 0));
+                };
+                auto wait_full = [&]() {
+                    if (!W.wait(bFULL + 8 * stage, phase)) return false;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                    return true;
+                };
+                auto wait_acc = [&](int h) {
+                    if (!W.template wait<true>(bTEMPTY + 8 * h, (h == 0 ? used0 : used1) & 1u)) return false;
+                    tc_fence_after_sync();
+                    return true;
+                };
+                for (int u = cluster_id; ok && u < p.total_units; u += num_clusters) {
+                    const Unit un = unit_of(u, p);
+                    if (un.half >= 0) {
+                        // half-width unit: one box, half 0 of the accumulator
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            const uint32_t s0 = stage;
+                            if (!wait_full()) { ok = false; break; }
+                            tc_fence_after_sync();
+                            if (kb == 0 && !wait_acc(0)) { ok = false; break; }
+                            mma_block(s0, 0, kb == 0);
+                            issued_any = true;
+                            tc_commit_2_mc(bEMPTY + 8 * s0, 0x3);
+                        }
+                        if (!ok) break;
+                        tc_commit_2_mc(bTFULL, 0x3);
+                        ++used0;
+                    } else if (nkb > 2 * J) {
+                        // head group: K blocks 0 .. J-1
+                        const uint32_t h0 = stage;
+#pragma unroll
+                        for (int j = 0; j < J; ++j)
+                            if (ok && !wait_full()) ok = false;
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        if (!wait_acc(0)) { ok = false; break; }
+#pragma unroll
+                        for (int j = 0; j < J; ++j) mma_block(slot(h0 + j), 0, j == 0);
+                        issued_any = true;
+                        if (!wait_acc(1)) { ok = false; break; }
+#pragma unroll
+                        for (int j = 0; j < J; ++j) mma_block(slot(h0 + j), 1, j == 0);
+#pragma unroll
+                        for (int j = 0; j < J; ++j) tc_commit_2_mc(bEMPTY + 8 * slot(h0 + j), 0x3);
+                        // the blocks in between: both halves back to back
+                        for (int kb = J; kb < nkb - J; ++kb) {
+                            const uint32_t s0 = stage;
+                            if (!wait_full()) { ok = false; break; }
+                            tc_fence_after_sync();
+                            mma_block(s0, 0, false);
+                            mma_block(s0, 1, false);
+                            tc_commit_2_mc(bEMPTY + 8 * s0, 0x3);
+                        }
+                        if (!ok) break;
+                        // tail group: K blocks nkb-J .. nkb-1
+                        const uint32_t t0 = stage;
+#pragma unroll
+                        for (int j = 0; j < J; ++j)
+                            if (ok && !wait_full()) ok = false;
+                        if (!ok) break;
+                        tc_fence_after_sync();
+#pragma unroll
+                        for (int j = 0; j < J; ++j) mma_block(slot(t0 + j), 0, false);
+                        tc_commit_2_mc(bTFULL, 0x3);          // half 0 of the accumulator is complete
+#pragma unroll
+                        for (int j = 0; j < J; ++j) mma_block(slot(t0 + j), 1, false);
+#pragma unroll
+                        for (int j = 0; j < J; ++j) tc_commit_2_mc(bEMPTY + 8 * slot(t0 + j), 0x3);
+                        tc_commit_2_mc(bTFULL + 8, 0x3);      // half 1 too
+                        ++used0;
+                        ++used1;
+                    } else {
+                        // few K blocks: every block holds both halves' MMAs; the
+                        // accumulator is taken before the first and released after
+                        // the last block
+                        for (int kb = 0; kb < nkb; ++kb) {
+                            const uint32_t s0 = stage;
+                            if (!wait_full()) { ok = false; break; }
+                            tc_fence_after_sync();
+                            if (kb == 0 && (!wait_acc(0) || !wait_acc(1))) { ok = false; break; }
+                            mma_block(s0, 0, kb == 0);
+                            mma_block(s0, 1, kb == 0);
+                            issued_any = true;
+                            tc_commit_2_mc(bEMPTY + 8 * s0, 0x3);
+                        }
+                        if (!ok) break;
+                        tc_commit_2_mc(bTFULL, 0x3);
+                        tc_commit_2_mc(bTFULL + 8, 0x3);
+                        ++used0;
+                        ++used1;
                     }
                 }
-                if (!ok) break;
-                // accumulator of this tile is complete
-                if constexpr (CG == 1) tc_commit_1(bTFULL + 8 * b);
-                else tc_commit_2_mc(bTFULL + 8 * b, 0x3);
             }
             if (issued_any) {
                 // all multiplies have finished before tensor memory is released
@@ -520,88 +668,134 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const int q = warp & 3;                  // tensor-memory lane quarter of this warp
         const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleEpilogue};
         const uint32_t tempty_leader = (CG == 2) ? mapa_shared(bTEMPTY, 0) : bTEMPTY;
-        // seed: both accumulator buffers start free
+        // seed: both accumulator event pairs start free (the two buffers of
+        // the 256 x 256 and 128 x 128 tiles, the two halves of the wide one)
         if (lane == 0) {
             for (int b = 0; b < 2; ++b) {
                 if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * b);
                 else mbar_arrive_cluster(tempty_leader + 8 * b);
             }
         }
-        uint32_t sbuf = 0;
-        // Writes 64 f16 columns (h: 32 packed pairs) of this lane's row of a
-        // 32-row block: through swizzled staging and a TMA store (clipped at M
-        // and N), or with guarded plain stores.
-        auto store_chunk = [&](const uint32_t(&h)[32], int row0, int col0) {
-            if (p.store == kStoreTma) {
-                const uint32_t buf = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF + sbuf * EPI_BUF;
-                // the store issued from this buffer two chunks ago has finished reading it
-                if (lane == 0) bulk_wait_group_read<1>();
-                __syncwarp();
-                const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128;
+        // Reads 64 accumulator columns (from tensor-memory address taddr) of
+        // this lane's row and rounds them to 32 packed f16 pairs.
+        auto load_chunk = [&](uint32_t taddr, uint32_t(&h)[32]) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(taddr, v0);
+            tmem_ld_32x32b_x32(taddr + 32, v1);
+            tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h[4 * j]),
-                                 "r"(h[4 * j + 1]), "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                // a box wholly past M or N (padding rows of a pair tile) is not stored
-                if (lane == 0 && row0 < p.M && col0 < p.N) {
-                    tma_store_2d(&tmC, buf, col0, row0);
-                    bulk_commit_group();
-                }
-                sbuf ^= 1u;
-            } else {
-                const int row = row0 + lane;
-                if (row < p.M) {
-                    unsigned short* dst = reinterpret_cast<unsigned short*>(p.out) + static_cast<int64_t>(row) * p.N;
+            for (int k = 0; k < 16; ++k) h[k] = pack_half2(v0[2 * k], v0[2 * k + 1]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = col0 + 2 * i;
-                        if (col < p.N) dst[col] = static_cast<unsigned short>(h[i] & 0xFFFFu);
-                        if (col + 1 < p.N) dst[col + 1] = static_cast<unsigned short>(h[i] >> 16);
-                    }
+            for (int k = 0; k < 16; ++k) h[16 + k] = pack_half2(v1[2 * k], v1[2 * k + 1]);
+        };
+        // Writes a chunk (this lane's row of a 32 x 64 block) into staging
+        // buffer `buf` in the 128-byte swizzle the output tensor map uses.
+        auto stage_chunk = [&](uint32_t buf, const uint32_t(&h)[32]) {
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ static_cast<uint32_t>(lane & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h[4 * j]), "r"(h[4 * j + 1]),
+                             "r"(h[4 * j + 2]), "r"(h[4 * j + 3])
+                             : "memory");
+            }
+        };
+        // Guarded plain stores of a chunk (outputs TMA cannot address).
+        auto store_direct = [&](const uint32_t(&h)[32], int row0, int col0) {
+            const int row = row0 + lane;
+            if (row < p.M) {
+                unsigned short* dst = reinterpret_cast<unsigned short*>(p.out) + static_cast<int64_t>(row) * p.N;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = col0 + 2 * i;
+                    if (col < p.N) dst[col] = static_cast<unsigned short>(h[i] & 0xFFFFu);
+                    if (col + 1 < p.N) dst[col + 1] = static_cast<unsigned short>(h[i] >> 16);
                 }
             }
         };
-        uint32_t tcount = 0;
-        for (int u = cluster_id; u < p.total_units; u += num_clusters, ++tcount) {
-            const Unit un = unit_of(u, p);
-            const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
+        // Waits for accumulator event pair i (parity `par`), writes its ncols
+        // columns starting at tensor-memory column acc_col0 to output columns
+        // col_base.. of rows row0..row0+31, and releases the columns.  False
+        // if the wait gave up.  With TMA stores the chunks go two at a time
+        // through the warp's two staging buffers: one wait for the buffers,
+        // one proxy fence and one bulk group per pair (measured per chunk on
+        // GB300: the fence and the store issue cost about as much as the
+        // tensor-memory load and the rounding together).
+        auto drain = [&](uint32_t i, uint32_t par, uint32_t acc_col0, int ncols, int row0, int col_base) {
             bool got = true;
-            if (lane == 0) got = W.wait(bTFULL + 8 * b, aph);
+            if (lane == 0) got = W.wait(bTFULL + 8 * i, par);
             got = __shfl_sync(0xffffffffu, got, 0);
-            if (!got) break;
+            if (!got) return false;
             tc_fence_after_sync();
-            int tm, tn;
-            tile_coords(un.tile, p, tm, tn);
-            const int row0 = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA + q * 32;
-            // a half-width unit holds UMMA_N / 2 accumulator columns, starting
-            // at column half * UMMA_N / 2 of its tile
-            const int ncols = un.half >= 0 ? SH::ACC_COLS / 2 : SH::ACC_COLS;
-            const int col_base = tn * SH::UMMA_N + (un.half > 0 ? SH::UMMA_N / 2 : 0);
-            for (int c = 0; c < ncols / EPI_COLS; ++c) {
-                uint32_t v0[32], v1[32];
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * SH::ACC_COLS +
-                                       static_cast<uint32_t>(c * EPI_COLS);
-                tmem_ld_32x32b_x32(taddr, v0);
-                tmem_ld_32x32b_x32(taddr + 32, v1);
-                tmem_ld_wait();
-                uint32_t h[32];
+            const int nch = ncols / EPI_COLS;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col0;
+            if (p.store == kStoreTma) {
+                const uint32_t bufs = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF;
+                for (int c = 0; c < nch; c += 2) {
+                    const int nb = nch - c < 2 ? nch - c : 2;
+                    // the stores issued from both buffers have finished reading them
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) h[i] = pack_half2(v0[2 * i], v0[2 * i + 1]);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) h[16 + i] = pack_half2(v1[2 * i], v1[2 * i + 1]);
-                store_chunk(h, row0, col_base + c * EPI_COLS);
+                    for (int t = 0; t < 2; ++t) {
+                        if (t < nb) {
+                            uint32_t h[32];
+                            load_chunk(tbase + static_cast<uint32_t>((c + t) * EPI_COLS), h);
+                            stage_chunk(bufs + t * EPI_BUF, h);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        bool any = false;
+                        for (int t = 0; t < nb; ++t) {
+                            const int col0 = col_base + (c + t) * EPI_COLS;
+                            // a box wholly past M or N (padding rows of a pair tile) is not stored
+                            if (row0 < p.M && col0 < p.N) {
+                                tma_store_2d(&tmC, bufs + t * EPI_BUF, col0, row0);
+                                any = true;
+                            }
+                        }
+                        if (any) bulk_commit_group();
+                    }
+                }
+            } else {
+                for (int c = 0; c < nch; ++c) {
+                    uint32_t h[32];
+                    load_chunk(tbase + static_cast<uint32_t>(c * EPI_COLS), h);
+                    store_direct(h, row0, col_base + c * EPI_COLS);
+                }
             }
-            // this warp's reads of accumulator buffer b are complete
+            // this warp's reads of these accumulator columns are complete
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
-                if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * b);
-                else mbar_arrive_cluster(tempty_leader + 8 * b);
+                if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * i);
+                else mbar_arrive_cluster(tempty_leader + 8 * i);
+            }
+            return true;
+        };
+        uint32_t tcount = 0;
+        uint32_t used0 = 0u, used1 = 0u;     // wide tile: units that have used half 0 / half 1
+        for (int u = cluster_id; u < p.total_units; u += num_clusters, ++tcount) {
+            const Unit un = unit_of(u, p);
+            int tm, tn;
+            tile_coords(un.tile, p, tm, tn);
+            const int row0 = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA + q * 32;
+            // a half-width unit holds HALF_N accumulator columns, starting at
+            // column half * HALF_N of its tile
+            const int col_base = tn * SH::TILE_N + (un.half > 0 ? SH::HALF_N : 0);
+            if constexpr (NW == 1) {
+                const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
+                const int ncols = un.half >= 0 ? SH::HALF_N : SH::ACC_COLS;
+                if (!drain(b, aph, b * SH::ACC_COLS, ncols, row0, col_base)) break;
+            } else {
+                if (!drain(0u, used0 & 1u, 0u, SH::UMMA_N, row0, col_base)) break;
+                ++used0;
+                if (un.half < 0) {
+                    if (!drain(1u, used1 & 1u, SH::UMMA_N, SH::UMMA_N, row0, col_base + SH::UMMA_N)) break;
+                    ++used1;
+                }
             }
         }
         if (lane == 0 && p.store == kStoreTma) bulk_wait_group<0>();
@@ -670,6 +864,7 @@ repack_rows_kernel(const uint16_t* __restrict__ a, int64_t ma, const uint16_t* _
 
 struct Plan {
     int cg = 1;
+    int nw = 1;                 // MMAs per K step (2: the wide 256 x 512 pair tile)
     bool repack = false;        // operands copied to 16-byte aligned rows, then TMA
     int producer = kProducerTma;
     int copy_bytes = 16;
@@ -678,17 +873,25 @@ struct Plan {
     int smem = 0;
 };
 
-template <int S>
-constexpr int dyn_smem() { return Layout<S>::DYN; }
+// The wide tile's 48 KB slots fit the shared memory up to this many stages.
+constexpr int WIDE_MAX_STAGES = 4;
 
-int smem_for(int stages) {
+int smem_for(int stages, int nw) {
+    if (nw == 2) {
+        switch (stages) {
+            case 1: return Layout<1, 2>::DYN;
+            case 2: return Layout<2, 2>::DYN;
+            case 3: return Layout<3, 2>::DYN;
+            default: return Layout<4, 2>::DYN;
+        }
+    }
     switch (stages) {
-        case 1: return dyn_smem<1>();
-        case 2: return dyn_smem<2>();
-        case 3: return dyn_smem<3>();
-        case 4: return dyn_smem<4>();
-        case 5: return dyn_smem<5>();
-        default: return dyn_smem<6>();
+        case 1: return Layout<1>::DYN;
+        case 2: return Layout<2>::DYN;
+        case 3: return Layout<3>::DYN;
+        case 4: return Layout<4>::DYN;
+        case 5: return Layout<5>::DYN;
+        default: return Layout<6>::DYN;
     }
 }
 
@@ -715,6 +918,13 @@ inline size_t repack_bytes(int64_t M, int64_t N, int64_t K, size_t* b_offset) {
     if (b_offset) *b_offset = a_bytes;
     return a_bytes + (static_cast<size_t>(N) * Kp * 2 + 255) / 256 * 256;
 }
+
+// Whether the wide pair tile (256 x 512) should replace the 256 x 256 one.  It
+// copies a quarter fewer operand bytes into shared memory per flop, which on
+// GB300 lets the power-capped clock run higher (measured 3-6 % faster from
+// 4096^3 up, and never slower).  It is not used where its 512-column tiles
+// would add a block of padding columns the 256-column tiles do not have.
+bool want_wide(int64_t N) { return (N + 511) / 512 * 2 == (N + 255) / 256; }
 
 // `allow_repack` = false plans the path that needs no scratch memory.
 Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, const void* out, int stages,
@@ -743,12 +953,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     const bool want_pair = (flags & GEMM_DEBUG_FORCE_PAIR_TILE) || 2 * pair_tiles >= num_sms;
     pl.cg = (pl.producer == kProducerTma && !(flags & GEMM_DEBUG_FORCE_SOLO_TILE) && want_pair) ? 2 : 1;
-    const int tile = 128 * pl.cg;
-    pl.tiles_m = static_cast<int>((M + tile - 1) / tile);
-    pl.tiles_n = static_cast<int>((N + tile - 1) / tile);
+    pl.nw = (pl.cg == 2 && stages <= WIDE_MAX_STAGES && !(flags & GEMM_DEBUG_FORCE_NARROW_TILE) &&
+             ((flags & GEMM_DEBUG_FORCE_WIDE_TILE) || want_wide(N)))
+                ? 2
+                : 1;
+    const int tile_m = 128 * pl.cg, tile_n = 128 * pl.cg * pl.nw;
+    pl.tiles_m = static_cast<int>((M + tile_m - 1) / tile_m);
+    pl.tiles_n = static_cast<int>((N + tile_n - 1) / tile_n);
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
     pl.num_kb = static_cast<int>((K + BK - 1) / BK);
-    pl.smem = smem_for(stages);
+    pl.smem = smem_for(stages, pl.nw);
     return pl;
 }
 
@@ -759,11 +973,11 @@ inline int block_threads(const Plan& pl) {
 // Sets the kernel's shared-memory limit (once per device) and returns how
 // many CTA groups (pairs or single CTAs) can be resident at once: the size of
 // the persistent grid.  0 on failure.
-template <int CG, int S>
+template <int CG, int S, int NW>
 int capacity(const DeviceInfo& info, int threads) {
-    auto kern = gemm_f16_nt_kernel<CG, S>;
-    constexpr int smem = Layout<S>::DYN;
-    static_assert(Layout<S>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
+    auto kern = gemm_f16_nt_kernel<CG, S, NW>;
+    constexpr int smem = Layout<S, NW>::DYN;
+    static_assert(Layout<S, NW>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
     static int configured[64] = {};
     static int max_clusters[64] = {};
     if (!configured[info.device]) {
@@ -796,31 +1010,37 @@ int capacity(const DeviceInfo& info, int threads) {
     }
 }
 
-template <int CG>
+template <int CG, int NW>
 int capacity_for(int stages, const DeviceInfo& info, int threads) {
     switch (stages) {
-        case 1: return capacity<CG, 1>(info, threads);
-        case 2: return capacity<CG, 2>(info, threads);
-        case 3: return capacity<CG, 3>(info, threads);
-        case 4: return capacity<CG, 4>(info, threads);
-        case 5: return capacity<CG, 5>(info, threads);
-        default: return capacity<CG, 6>(info, threads);
+        case 1: return capacity<CG, 1, NW>(info, threads);
+        case 2: return capacity<CG, 2, NW>(info, threads);
+        case 3: return capacity<CG, 3, NW>(info, threads);
+        case 4: return capacity<CG, 4, NW>(info, threads);
     }
+    if constexpr (NW == 1) return stages == 5 ? capacity<CG, 5, 1>(info, threads) : capacity<CG, 6, 1>(info, threads);
+    return 0;
+}
+
+int capacity_of(const Plan& pl, int stages, const DeviceInfo& info) {
+    const int threads = block_threads(pl);
+    if (pl.cg == 1) return capacity_for<1, 1>(stages, info, threads);
+    return pl.nw == 2 ? capacity_for<2, 2>(stages, info, threads) : capacity_for<2, 1>(stages, info, threads);
 }
 
 // Launches the persistent grid: one CTA group per work unit, at most as many
 // as can be resident.
-template <int CG, int S>
+template <int CG, int S, int NW>
 int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
            const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
-    auto kern = gemm_f16_nt_kernel<CG, S>;
+    auto kern = gemm_f16_nt_kernel<CG, S, NW>;
     const int threads = block_threads(pl);
-    const int cap = capacity<CG, S>(info, threads);
+    const int cap = capacity<CG, S, NW>(info, threads);
     if (cap <= 0) return GEMM_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = Layout<S>::DYN;
+    cfg.dynamicSmemBytes = Layout<S, NW>::DYN;
     cfg.stream = stream;
     if constexpr (CG == 2) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -839,18 +1059,27 @@ int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const 
     return GEMM_OK;
 }
 
-template <int CG>
+template <int CG, int NW>
 int launch_stages(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
                   const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
     switch (stages) {
-        case 1: return launch<CG, 1>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 2: return launch<CG, 2>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 3: return launch<CG, 3>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 4: return launch<CG, 4>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 5: return launch<CG, 5>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 6: return launch<CG, 6>(pl, info, ta, tb, tbh, tc, p, stream);
-        default: return GEMM_ERR_UNSUPPORTED_STAGES;
+        case 1: return launch<CG, 1, NW>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 2: return launch<CG, 2, NW>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 3: return launch<CG, 3, NW>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 4: return launch<CG, 4, NW>(pl, info, ta, tb, tbh, tc, p, stream);
     }
+    if constexpr (NW == 1) {
+        if (stages == 5) return launch<CG, 5, 1>(pl, info, ta, tb, tbh, tc, p, stream);
+        if (stages == 6) return launch<CG, 6, 1>(pl, info, ta, tb, tbh, tc, p, stream);
+    }
+    return GEMM_ERR_UNSUPPORTED_STAGES;
+}
+
+int launch_plan(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
+                const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
+    if (pl.cg == 1) return launch_stages<1, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    return pl.nw == 2 ? launch_stages<2, 2>(stages, pl, info, ta, tb, tbh, tc, p, stream)
+                      : launch_stages<2, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
 }
 
 }  // namespace f16nt
@@ -864,7 +1093,7 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
     if (!plan) return GEMM_ERR_INVALID_ARG;
     const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, pws::sm_count_or_default(), pws::debug_flags());
     plan[0] = 128 * pl.cg;
-    plan[1] = 128 * pl.cg;
+    plan[1] = 128 * pl.cg * pl.nw;
     plan[2] = BK;
     plan[3] = pl.cg;
     plan[4] = pl.repack ? 2 : pl.producer;
@@ -969,25 +1198,24 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     // Tail split: when the tiles leave a last, partial wave of the persistent
     // grid (or fewer tiles than the grid) and twice that many units still
     // fit in one wave, each of those tiles runs as two half-width units on the
-    // wave's otherwise idle CTA groups.  Only the TMA producer supports it (it
-    // needs the 64-row B box).  Each output element is still one in-order K
-    // sum; the decision depends on the shape and the device, never on S.
+    // wave's otherwise idle CTA groups.  Only the TMA producer supports it
+    // (the 256 x 256 and 128 x 128 tiles need a 64-row B box; a half of the
+    // wide tile is one ordinary box).  Each output element is still one
+    // in-order K sum; the decision depends on the shape and the device, never
+    // on S.
     CUtensorMap tbh;
     memset(&tbh, 0, sizeof(tbh));
-    const int cap = pl.cg == 2 ? capacity_for<2>(stages, info, block_threads(pl))
-                               : capacity_for<1>(stages, info, block_threads(pl));
+    const int cap = capacity_of(pl, stages, info);
     if (cap <= 0) return done(GEMM_ERR_LAUNCH);
     const int waves = pl.num_tiles / cap;
     const int tail = pl.num_tiles - waves * cap;
     if (pl.producer == kProducerTma && tail > 0 && 2 * tail <= cap && !(flags & GEMM_DEBUG_NO_SPLIT)) {
-        if (!encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return done(GEMM_ERR_LAUNCH);
+        if (pl.nw == 1 && !encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return done(GEMM_ERR_LAUNCH);
         p.full_units = waves * cap;
         p.split = 2;
         p.total_units = waves * cap + 2 * tail;
     }
-    const int rc2 = pl.cg == 2 ? launch_stages<2>(stages, pl, info, ta, tb, tbh, tc, p, stream)
-                               : launch_stages<1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
-    return done(rc2);
+    return done(launch_plan(stages, pl, info, ta, tb, tbh, tc, p, stream));
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -1113,6 +1341,5 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     p.total_units = pl.num_tiles;
     CUtensorMap tbh;                    // unused without the tail split
     memset(&tbh, 0, sizeof(tbh));
-    if (pl.cg == 2) return launch_stages<2>(stages, pl, info, ta, tb, tbh, tc, p, stream);
-    return launch_stages<1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    return launch_plan(stages, pl, info, ta, tb, tbh, tc, p, stream);
 }

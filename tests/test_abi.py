@@ -86,16 +86,41 @@ def test_debug_flags_and_timeout_setters(lib):
 
 def test_plan_headline_shapes(lib):
     pws.gemm_set_debug_flags(0)
+    # five and six slots: the 256 x 256 pair tile, 32 KB slots
     p = pws.gemm_f16_nt_plan(8192, 8192, 8192, stages=6)
     assert (p["bm"], p["bn"], p["bk"], p["cta_group"]) == (256, 256, 64, 2)
     assert p["producer"] == 0 and p["store"] == 0
     assert p["tiles"] == 32 * 32 and p["k_blocks"] == 128
-    # ring slots of 32 KB per CTA plus 32 KB of epilogue staging fit the 227 KB limit for every S
+    assert {k: v for k, v in pws.gemm_f16_nt_plan(8192, 8192, 8192, stages=5).items() if k != "smem_bytes"} == \
+        {k: v for k, v in p.items() if k != "smem_bytes"}
+    # one to four slots: the wide 256 x 512 pair tile, 48 KB slots (A and two B boxes per CTA)
     for s in range(1, 7):
         q = pws.gemm_f16_nt_plan(8192, 8192, 8192, stages=s)
-        assert q["smem_bytes"] <= 232448
-        assert q["smem_bytes"] >= s * 32768 + 32768
-        assert {k: v for k, v in q.items() if k != "smem_bytes"} == {k: v for k, v in p.items() if k != "smem_bytes"}
+        slot = 49152 if s <= 4 else 32768
+        assert q["bn"] == (512 if s <= 4 else 256)
+        assert q["tiles"] == 32 * (16 if s <= 4 else 32)
+        # ring slots plus 32 KB of epilogue staging fit the 227 KB limit for every S
+        assert s * slot + 32768 <= q["smem_bytes"] <= 232448
+
+
+def test_plan_wide_tile_rule(lib):
+    # the wide tile is used where its 512-column tiles add no padded block of 256 columns
+    for n, wide in ((8192, True), (3000, True), (512, True), (4608, True), (256, False), (768, False),
+                    (1100, False), (257, True)):
+        q = pws.gemm_f16_nt_plan(32768, n, 1024, stages=4)      # M large enough for the pair tile
+        assert q["cta_group"] == 2 and (q["bn"] == 512) == wide, n
+    # the debug flags override it either way; six slots never fit the wide tile
+    try:
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_NARROW_TILE)
+        assert pws.gemm_f16_nt_plan(8192, 8192, 8192, stages=4)["bn"] == 256
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_WIDE_TILE)
+        assert pws.gemm_f16_nt_plan(32768, 256, 1024, stages=4)["bn"] == 512
+        assert pws.gemm_f16_nt_plan(32768, 256, 1024, stages=6)["bn"] == 256
+        # the single-CTA tile has no wide form
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_WIDE_TILE | pws.GEMM_DEBUG_FORCE_SOLO_TILE)
+        assert (pws.gemm_f16_nt_plan(4096, 4096, 1024, stages=4)["bn"], pws.gemm_f16_nt_plan(4096, 4096, 1024, stages=4)["cta_group"]) == (128, 1)
+    finally:
+        pws.gemm_set_debug_flags(0)
 
 
 def test_plan_ragged_shape(lib):
@@ -104,8 +129,9 @@ def test_plan_ragged_shape(lib):
     p = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
     assert p["producer"] == 2 and p["copy_bytes"] == 16
     assert p["cta_group"] == 2 and p["bm"] == 256               # 16 x 12 pair tiles >= 152 / 2
+    assert p["bn"] == 512                       # N = 3000: 6 wide tile columns pad no more than 12 narrow ones
     assert p["store"] == 0                      # 6000-byte output rows are 16-byte aligned
-    assert p["tiles"] == 16 * 12 and p["k_blocks"] == 33
+    assert p["tiles"] == 16 * 6 and p["k_blocks"] == 33
     # the async-copy producer reads them in place (single-CTA tile, 4-byte copies)
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
     try:

@@ -182,7 +182,7 @@ def test_f16_edge_shapes(M, N, K, flags):
 
 @pytest.mark.parametrize("M,N,K,flags", [
     (1024, 1024, 1024, 0),                                # 64 single tiles < 152 SMs: every tile split in 2
-    (700, 650, 1000, pws.GEMM_DEBUG_FORCE_PAIR_TILE),     # 9 pair tiles: split in 4 (>= 4 K blocks each)
+    (700, 650, 1000, pws.GEMM_DEBUG_FORCE_PAIR_TILE),     # 9 pair tiles < 76 pairs: every tile split in 2
     (2300, 2100, 768, 0),                                 # 9 x 9 pair tiles = 81 > 76: a 5-tile tail split
 ])
 def test_f16_tail_split_matches_unsplit(M, N, K, flags):
@@ -192,9 +192,59 @@ def test_f16_tail_split_matches_unsplit(M, N, K, flags):
     split = run_f16(a, b, 3, flags)
     whole = run_f16(a, b, 3, flags | pws.GEMM_DEBUG_NO_SPLIT)
     assert_f16_ok(split, ref, K)
-    assert_f16_ok(whole, ref, K)
-    # the split changes only the fp32 summation order: the two agree under the same rule
-    assert_f16_ok(split, whole.astype(np.float64), K)
+    # a half-width unit runs the whole K loop for its columns: same sums, same order
+    assert np.array_equal(split.view(np.uint16), whole.view(np.uint16))
+
+
+WIDE = pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE
+NARROW = pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_NARROW_TILE
+
+
+def test_f16_wide_tile_bitwise_equals_narrow_and_solo():
+    # 3 x 3 wide tiles: ragged M (700 = 2 x 256 + 188), N = 1100 leaves a last
+    # tile column of 76 (its second B box wholly past N), K has a tail of 40
+    M, N, K = 700, 1100, 1000
+    a = inputs.uniform_f16(41, 0, (M, K))
+    b = inputs.uniform_f16(41, 1, (N, K))
+    narrow = run_f16(a, b, 3, NARROW)
+    solo = run_f16(a, b, 3, pws.GEMM_DEBUG_FORCE_SOLO_TILE)
+    assert_f16_ok(narrow, oracle.gemm_f16_nt_f64(a, b), K)
+    # every tiling sums each element over K in the same order
+    assert np.array_equal(solo.view(np.uint16), narrow.view(np.uint16))
+    for s in range(1, 5):
+        for extra in (0, pws.GEMM_DEBUG_NO_SPLIT):
+            wide = run_f16(a, b, s, WIDE | extra)
+            assert np.array_equal(wide.view(np.uint16), narrow.view(np.uint16)), f"wide S={s} flags={extra}"
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 8), (5, 3, 64),                 # one tile, almost all padding
+    (260, 300, 136),                       # the peer CTA's rows and the second B box past M and N
+    (256, 512, 64), (257, 513, 72),        # exact tile, and one row / column over
+    (513, 257, 200), (300, 1030, 72),
+    (700, 1100, 2050),                     # repacked operands into the wide tile
+])
+def test_f16_wide_tile_edge_shapes(M, N, K):
+    a = inputs.normal_f16(M * 5 + K, 0, (M, K))
+    b = inputs.normal_f16(N * 11 + K, 1, (N, K))
+    ref = oracle.gemm_f16_nt_f64(a, b)
+    for s in (1, 2, 4):
+        assert_f16_ok(run_f16(a, b, s, WIDE), ref, K)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1024, 1024, 512),      # 4 x 2 wide tiles, fewer than the CTA pairs: all split into halves
+    (2300, 4600, 256),      # 9 x 9 = 81 wide tiles: one full wave and a tail of 5 split into halves
+])
+def test_f16_wide_tile_tail_split(M, N, K):
+    a = inputs.uniform_f16(M + N + 7, 0, (M, K))
+    b = inputs.uniform_f16(M + N + 7, 1, (N, K))
+    split = run_f16(a, b, 4, WIDE)
+    whole = run_f16(a, b, 4, WIDE | pws.GEMM_DEBUG_NO_SPLIT)
+    narrow = run_f16(a, b, 4, NARROW | pws.GEMM_DEBUG_NO_SPLIT)
+    assert np.array_equal(split.view(np.uint16), whole.view(np.uint16))
+    assert np.array_equal(split.view(np.uint16), narrow.view(np.uint16))
+    assert_f16_ok(split, oracle.gemm_f16_nt_f64(a, b), K)
 
 
 def test_f16_k_zero_and_empty():
