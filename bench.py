@@ -30,6 +30,7 @@ With torchrun (N > 1) every rank runs an independent replica of the workload
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -110,7 +111,11 @@ def profiled_traffic(M, N, K, S):
 
 class ClockSampler:
     """nvidia-smi clock / throttle samples taken while the timed region runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    # nvidia-smi's own sample time comes first: lines written to a pipe can
+    # reach us in bursts, so their arrival time does not place them
+    # (power.draw is a one-second average on this GPU generation, too slow for
+    # a timed region of under a second; power.draw.instant is the sample)
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -146,20 +151,26 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = [ln for ts, ln in self.lines if t0 - 0.06 <= ts <= t1 + 0.06] or [ln for _, ln in self.lines[-3:]]
+        def sample_time(ln, arrived):
+            try:        # local time, as time.time() sees it on the same machine
+                return datetime.datetime.strptime(ln.split(",")[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return arrived
+        rows = [ln for ts, ln in self.lines if t0 - 0.06 <= sample_time(ln, ts) <= t1 + 0.06] or \
+            [ln for _, ln in self.lines[-3:]]
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in rows:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+                power.append(float(f[4]))
             except ValueError:
                 continue
-            for name, v in zip(names, f[5:9]):
+            for name, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,

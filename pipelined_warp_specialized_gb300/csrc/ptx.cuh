@@ -53,14 +53,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 
 // One probe of the phase with the given parity (true once it has completed).
+// A thread whose try_wait finds the phase incomplete is suspended until the
+// phase completes or this many nanoseconds pass (the PTX suspend-time hint),
+// instead of a shorter system-dependent limit.  The callers' loops re-check
+// their abort flag and time limit between tries.  Fewer wake-ups of idle
+// waiters measured 0.5-0.8 % faster at 8192^3 on the power-capped GB300.
+constexpr int kTryWaitSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kTryWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -71,10 +78,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kTryWaitSuspendNs)
         : "memory");
     return ok != 0;
 }
