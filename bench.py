@@ -50,7 +50,8 @@ from pipelined_warp_specialized_gb300 import inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_f16_nt_8192_traffic.txt")
-KERNEL_SOURCE = os.path.join(ROOT, "pipelined_warp_specialized_gb300", "csrc", "gemm_f16_nt.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "pipelined_warp_specialized_gb300", "csrc", f)
+                  for f in ("gemm_f16_nt.cu", "ptx.cuh", "internal.h")]
 
 
 # ---------------------------------------------------------------- helpers
@@ -83,8 +84,12 @@ def measured_peaks():
 
 
 def kernel_sha() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of sha256 over every source the f16 kernel compiles from."""
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(M, N, K, S):

@@ -72,10 +72,14 @@ constexpr int BN_CTA = 128;            // B rows per CTA
 constexpr int A_SLOT = BM_CTA * BK * 2;
 constexpr int B_SLOT = BN_CTA * BK * 2;
 constexpr int SLOT_BYTES = A_SLOT + B_SLOT;   // 32 KB
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 4;           // epilogue warps: one per tensor-memory lane quarter, two staging buffers each
+constexpr int EPI_WARPS_WIDE = 8;      // the wide tile's: two per lane quarter, one staging buffer each
 constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128 bytes of f16)
 constexpr int EPI_BUF = 32 * EPI_COLS * 2;     // 32 rows x 64 columns
 constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+static_assert(EPI_WARPS_WIDE * EPI_BUF == EPI_BYTES, "both epilogue forms use the same staging bytes");
+template <int NW>
+constexpr int epi_warps() { return NW == 2 ? EPI_WARPS_WIDE : EPI_WARPS; }
 constexpr int MAX_STAGES = 6;
 constexpr int COPY_WARPS = 8;          // producer warps of the cp.async producer
 constexpr int COPY_THREADS = COPY_WARPS * 32;
@@ -334,7 +338,7 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
 // A CTA pair is always fed by TMA (one producer warp): its bound lets the
 // compiler use the registers the cp.async producer's eight warps would need.
 template <int CG, int S, int NW>
-__global__ void __launch_bounds__((CG == 2 ? 1 + 1 + EPI_WARPS : COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
+__global__ void __launch_bounds__((CG == 2 ? 1 + 1 + epi_warps<NW>() : COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ Params p) {
@@ -349,7 +353,8 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int P = static_cast<int>(blockDim.x / 32) - 1 - EPI_WARPS;   // producer warps
+    constexpr int EW = epi_warps<NW>();
+    const int P = static_cast<int>(blockDim.x / 32) - 1 - EW;          // producer warps
     const int mma_warp = P;
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
     const int cluster_id = blockIdx.x / CG;
@@ -371,7 +376,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bTFULL + 8 * b, 1);
-            mbar_init(bTEMPTY + 8 * b, EPI_WARPS * CG);
+            mbar_init(bTEMPTY + 8 * b, EW * CG);
         }
         mbar_init(bDRAIN, 1);
         *abort_flag = 0u;
@@ -664,7 +669,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         __syncwarp();
     } else {
         // ======================================================== epilogue
-        const int e = warp - P - 1;              // 0..3
+        const int e = warp - P - 1;              // 0 .. EW-1
         const int q = warp & 3;                  // tensor-memory lane quarter of this warp
         const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleEpilogue};
         const uint32_t tempty_leader = (CG == 2) ? mapa_shared(bTEMPTY, 0) : bTEMPTY;
@@ -729,7 +734,28 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             tc_fence_after_sync();
             const int nch = ncols / EPI_COLS;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col0;
-            if (p.store == kStoreTma) {
+            // the wide tile's two warps of a lane quarter take half of the chunks each
+            const int cb = NW == 2 ? (e / 4) * (nch / 2) : 0;
+            const int ce = NW == 2 ? cb + nch / 2 : nch;
+            if (NW == 2 && p.store == kStoreTma) {
+                // one staging buffer per warp
+                const uint32_t buf = sEPI + static_cast<uint32_t>(e) * EPI_BUF;
+                for (int c = cb; c < ce; ++c) {
+                    // the store issued from the buffer has finished reading it
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+                    uint32_t h[32];
+                    load_chunk(tbase + static_cast<uint32_t>(c * EPI_COLS), h);
+                    stage_chunk(buf, h);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    const int col0 = col_base + c * EPI_COLS;
+                    if (lane == 0 && row0 < p.M && col0 < p.N) {
+                        tma_store_2d(&tmC, buf, col0, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (p.store == kStoreTma) {
                 const uint32_t bufs = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF;
                 for (int c = 0; c < nch; c += 2) {
                     const int nb = nch - c < 2 ? nch - c : 2;
@@ -760,7 +786,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     }
                 }
             } else {
-                for (int c = 0; c < nch; ++c) {
+                for (int c = cb; c < ce; ++c) {
                     uint32_t h[32];
                     load_chunk(tbase + static_cast<uint32_t>(c * EPI_COLS), h);
                     store_direct(h, row0, col_base + c * EPI_COLS);
@@ -967,7 +993,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
 }
 
 inline int block_threads(const Plan& pl) {
-    return ((pl.producer == kProducerTma ? 1 : COPY_WARPS) + 1 + EPI_WARPS) * 32;
+    return ((pl.producer == kProducerTma ? 1 : COPY_WARPS) + 1 + (pl.nw == 2 ? EPI_WARPS_WIDE : EPI_WARPS)) * 32;
 }
 
 // Sets the kernel's shared-memory limit (once per device) and returns how
