@@ -21,7 +21,9 @@ Prints ONE JSON line (rank 0):
   clocks                -- nvidia-smi samples taken during the timed region
   configs               -- the other workloads (kernel-only timings): s32 NN
                            128x256x256, f16 NT 1024^3 S=2, 4096^3 S=4, the
-                           ragged 4000x3000x2050 S=3 and the 8192^3 S=1..6 sweep
+                           ragged 4000x3000x2050 S=3 and the 8192^3 S=1..6 sweep,
+                           and 16 independent 1024^3 f16 / s32 GEMMs issued
+                           on 1, 2, 4 or 8 streams (host concurrency)
 
 --impl reference times the CPU oracle instead (the slow reference arm).
 With torchrun (N > 1) every rank runs an independent replica of the workload
@@ -281,6 +283,40 @@ def e2e_pipelined(pws, torch, dev, a_h, b_h, c_h, stages, n_steps, warmup=2):
     return e0.elapsed_time(e1) / n_steps
 
 
+def concurrency_configs(pws, torch, G=16, stream_counts=(1, 2, 4, 8)):
+    """Host concurrency: G independent GEMMs of one small shape, issued
+    round-robin on n streams (fork from one stream, join back), captured in a
+    CUDA graph so that the GPU, not the host's launch cost, decides how much
+    of them overlaps.  Reported per batch of G."""
+    out = {}
+    dev = torch.device("cuda")
+    wl = inputs.WORKLOADS["f16_nt_1024"]
+    a, b = torch.from_numpy(wl.lhs()).to(dev), torch.from_numpy(wl.rhs()).to(dev)
+    outs = [torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev) for _ in range(G)]
+    wl2 = inputs.WORKLOADS["s32_nn_128x256x256"]
+    a2, b2 = torch.from_numpy(wl2.lhs()).to(dev), torch.from_numpy(wl2.rhs()).to(dev)
+    outs2 = [torch.empty(wl2.M, wl2.N, dtype=torch.int32, device=dev) for _ in range(G)]
+    cases = [(wl, "TFLOP_s", lambda i, st: pws.gemm_f16_nt(a, b, outs[i], stages=wl.stages[0], stream=st)),
+             (wl2, "TOPS", lambda i, st: pws.gemm_s32_nn(a2, b2, outs2[i], stream=st))]
+    for w, unit, call in cases:
+        res = {}
+        for ns in stream_counts:
+            streams = [torch.cuda.Stream() for _ in range(ns)]
+
+            def batch(s0, streams=streams, call=call):
+                for st in streams:
+                    st.wait_stream(s0)
+                for i in range(G):
+                    call(i, streams[i % len(streams)])
+                for st in streams:
+                    s0.wait_stream(st)
+
+            ms = time_graph(batch, torch, per_graph=4, replays=20)
+            res[f"streams{ns}"] = {"us_per_batch": round(ms * 1e3, 1), unit: round(G * w.flops / ms / 1e9, 2)}
+        out[f"{w.name}/x{G}_concurrent"] = res
+    return out
+
+
 def extra_configs(pws, torch, stream, reps=20):
     """Kernel-only timings of every workload (inputs resident)."""
     out = {}
@@ -333,6 +369,7 @@ def extra_configs(pws, torch, stream, reps=20):
                 pws.gemm_set_debug_flags(0)
             out[name + ("/" + suffix if suffix else "")] = res
         del a, b, c
+    out.update(concurrency_configs(pws, torch))
     return out
 
 

@@ -355,6 +355,61 @@ def test_f16_repack_scratch_is_stream_ordered():
             assert_f16_ok(o.cpu().numpy(), ref, K)
 
 
+def test_concurrent_gemms_on_four_streams():
+    # independent f16 GEMMs (single-CTA, 256x256 and wide pair tiles, S = 1..4)
+    # and s32 GEMMs issued round-robin on four streams forked from one, first
+    # eagerly, then captured as one fork/join graph and replayed
+    f16_cases = []
+    for i, (M, N, K) in enumerate([(300, 260, 200), (1024, 1024, 256), (4096, 4096, 64), (2304, 4608, 128),
+                                   (700, 1100, 320)]):
+        a = inputs.uniform_f16(70 + i, 0, (M, K))
+        b = inputs.uniform_f16(70 + i, 1, (N, K))
+        f16_cases.append((_dev(a), _dev(b), oracle.gemm_f16_nt_f64(a, b), K,
+                          torch.empty(M, N, dtype=torch.float16, device="cuda")))
+    s32_cases = []
+    for i, (M, N, K) in enumerate([(128, 256, 256), (17, 33, 15), (300, 500, 77)]):
+        a = inputs.ints(80 + i, 0, (M, K), -1000, 1000)
+        b = inputs.ints(80 + i, 1, (K, N), -1000, 1000)
+        s32_cases.append((_dev(a), _dev(b), oracle.gemm_s32_nn(a, b), torch.empty(M, N, dtype=torch.int32, device="cuda")))
+    streams = [torch.cuda.Stream() for _ in range(4)]
+
+    def launch_all(s0):
+        for st in streams:
+            st.wait_stream(s0)
+        j = 0
+        for da, db, _, _, o in f16_cases:
+            pws.gemm_f16_nt(da, db, o, stages=j % 4 + 1, stream=streams[j % 4])
+            j += 1
+        for da, db, _, o in s32_cases:
+            pws.gemm_s32_nn(da, db, o, stream=streams[j % 4])
+            j += 1
+        for st in streams:
+            s0.wait_stream(st)
+
+    def check_and_clear():
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_OK
+        for _, _, ref, K, o in f16_cases:
+            assert_f16_ok(o.cpu().numpy(), ref, K)
+            o.zero_()
+        for _, _, ref, o in s32_cases:
+            assert np.array_equal(o.cpu().numpy(), ref)
+            o.zero_()
+        torch.cuda.synchronize()
+
+    s0 = torch.cuda.Stream()
+    s0.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s0):
+        launch_all(s0)
+    check_and_clear()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s0):
+        launch_all(s0)
+    for _ in range(2):
+        g.replay()
+        check_and_clear()
+
+
 def test_f16_8192_sweep_identical_across_stages():
     wl = inputs.WORKLOADS["f16_nt_8192"]
     a, b = wl.lhs(), wl.rhs()
