@@ -396,6 +396,12 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     if constexpr (CG == 2) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched as a programmatic dependent: everything above (barriers, tensor
+    // memory, cluster) overlapped the previous grid's tail; global memory is
+    // touched only after that grid's writes are visible.  The next grid may
+    // start its own set-up as soon as SMs free up.
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     const bool is_leader = (CG == 1) || rank == 0;
 
@@ -1064,20 +1070,18 @@ int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const 
     const int cap = capacity<CG, S, NW>(info, threads);
     if (cap <= 0) return GEMM_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = Layout<S, NW>::DYN;
     cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if constexpr (CG == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    } else {
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     const int groups = p.total_units < cap ? p.total_units : cap;
     cfg.gridDim = dim3(CG * groups, 1, 1);

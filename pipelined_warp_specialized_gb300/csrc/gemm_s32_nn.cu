@@ -42,6 +42,9 @@ gemm_s32_nn_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, const i
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * BN;
     const int T = (K + BK - 1) / BK;
+    // launched as a programmatic dependent: the previous grid's writes first
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     // Issue the copies of K tile `t` into buffer `buf` (zero-fill outside M, N, K).
     auto issue = [&](int t, int buf) {
@@ -129,14 +132,13 @@ cudaError_t launch_tile(int M, int N, int K, const int32_t* lhs, const int32_t* 
     // 16-byte copies need 16-byte aligned rows; otherwise one element per copy.
     const bool b_vec = b16 && BN % 4 == 0;
     if (a16 && b_vec)
-        gemm_s32_nn_kernel<BM, BN, TM, TN, 16, 16><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+        return launch_pdl(gemm_s32_nn_kernel<BM, BN, TM, TN, 16, 16>, grid, dim3(THREADS), 0, stream, M, N, K, lhs, rhs, out);
     else if (a16)
-        gemm_s32_nn_kernel<BM, BN, TM, TN, 16, 4><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+        return launch_pdl(gemm_s32_nn_kernel<BM, BN, TM, TN, 16, 4>, grid, dim3(THREADS), 0, stream, M, N, K, lhs, rhs, out);
     else if (b_vec)
-        gemm_s32_nn_kernel<BM, BN, TM, TN, 4, 16><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
+        return launch_pdl(gemm_s32_nn_kernel<BM, BN, TM, TN, 4, 16>, grid, dim3(THREADS), 0, stream, M, N, K, lhs, rhs, out);
     else
-        gemm_s32_nn_kernel<BM, BN, TM, TN, 4, 4><<<grid, THREADS, 0, stream>>>(M, N, K, lhs, rhs, out);
-    return cudaGetLastError();
+        return launch_pdl(gemm_s32_nn_kernel<BM, BN, TM, TN, 4, 4>, grid, dim3(THREADS), 0, stream, M, N, K, lhs, rhs, out);
 }
 
 }  // namespace s32nn
@@ -224,6 +226,9 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, int S, const int32_t* __restrict__ 
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * BN;
     const int T = (K + BK - 1) / BK;
+    // launched as a programmatic dependent: the previous grid's writes first
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     auto issue = [&](int t, int slot) {
         const int k0 = t * BK;
@@ -304,7 +309,7 @@ cudaError_t launch_ring(int M, int N, int K, int S, const int32_t* lhs, const in
                 return cudaGetLastError();
             configured16[device] = true;
         }
-        k<<<grid, THREADS, smem, stream>>>(M, N, K, S, lhs, rhs, out);
+        return launch_pdl(k, grid, dim3(THREADS), smem, stream, M, N, K, S, lhs, rhs, out);
     } else {
         auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, 4>;
         if (!configured4[device]) {
@@ -312,9 +317,8 @@ cudaError_t launch_ring(int M, int N, int K, int S, const int32_t* lhs, const in
                 return cudaGetLastError();
             configured4[device] = true;
         }
-        k<<<grid, THREADS, smem, stream>>>(M, N, K, S, lhs, rhs, out);
+        return launch_pdl(k, grid, dim3(THREADS), smem, stream, M, N, K, S, lhs, rhs, out);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace s32nn

@@ -35,6 +35,34 @@ unsigned debug_flags();
 // SM count of the current device if one is present, else the GB300 count.
 int sm_count_or_default();
 
+// The launch attribute of programmatic dependent launch: the grid may be
+// scheduled while the previous grid in the stream finishes (its kernel calls
+// grid_dependency_wait() before any global memory access), so the launch
+// latency and the set-up overlap the previous grid's tail.
+inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
+#ifdef __CUDACC__
+// Launches `kernel` with the programmatic-dependent-launch attribute.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
+
 // Encodes a 2-D tiled tensor map over a row-major matrix of 2-byte elements:
 // `inner` elements per row, `outer` rows, `row_bytes` between rows; a box of
 // box_inner x box_outer elements with the 128-byte swizzle; out-of-bounds

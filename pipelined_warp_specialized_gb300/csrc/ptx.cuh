@@ -106,6 +106,20 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- grid dependencies
+//
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may be scheduled while the previous grid in the stream is
+// still running.  It must not touch global memory before
+// grid_dependency_wait(), which returns once the previous grid has completed
+// and its memory operations are visible (at once for a grid launched
+// without the attribute).  allow_dependent_launch() lets the next grid in
+// the stream be scheduled before this one finishes.
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- proxies
 
 // Orders this thread's generic-proxy shared-memory accesses against later
