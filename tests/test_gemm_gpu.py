@@ -410,6 +410,57 @@ def test_concurrent_gemms_on_four_streams():
         check_and_clear()
 
 
+@pytest.mark.parametrize("M,stages", [(1024, 2), (4096, 4)], ids=["single_tile", "wide_tile"])
+def test_dependent_f16_chain_reads_completed_outputs(M, stages):
+    # x <- f16(x . W^T) six times on one stream: each GEMM reads the previous
+    # one's output.  Every kernel lets the next grid be scheduled while it runs
+    # (programmatic dependent launch); the next one must still read the
+    # completed output.  Each step is checked against the oracle applied to the
+    # previous step's GPU output.  W is scaled by 1/32 (exact in f16) so the
+    # values neither overflow nor vanish over the chain.
+    K = M
+    w = (inputs.uniform_f16(90, 0, (K, K)).astype(np.float32) / 32).astype(np.float16)
+    x = inputs.uniform_f16(91, 0, (M, K))
+    dw = _dev(w)
+    cur = _dev(x)
+    outs = []
+    for _ in range(6):
+        cur = pws.gemm_f16_nt(cur, dw, stages=stages)
+        outs.append(cur)
+    torch.cuda.synchronize()
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    prev = x
+    for i, o in enumerate(outs):
+        got = o.cpu().numpy()
+        if M > 2048:     # the oracle on sampled entries at the large size
+            rows, cols = _sampled_entries(M, M, 50 + i, 4000, tile=256)
+            assert_f16_ok(got[rows, cols], oracle.gemm_f16_nt_entries(prev, w, rows, cols), K)
+        else:
+            assert_f16_ok(got, oracle.gemm_f16_nt_f64(prev, w), K)
+        assert np.abs(got.astype(np.float32)).max() > 1e-3, f"step {i} vanished"
+        prev = got
+
+
+def test_dependent_s32_chain_reads_completed_outputs():
+    # c <- c . B four times on one stream (wrapping int32), each step bit-exact
+    # against the oracle applied to the previous step's GPU output
+    n = 512
+    b = inputs.ints(92, 1, (n, n), -3, 3)
+    c = inputs.ints(92, 0, (n, n), -3, 3)
+    db = _dev(b)
+    cur = _dev(c)
+    outs = []
+    for _ in range(4):
+        cur = pws.gemm_s32_nn(cur, db)
+        outs.append(cur)
+    torch.cuda.synchronize()
+    prev = c
+    for o in outs:
+        got = o.cpu().numpy()
+        assert np.array_equal(got, oracle.gemm_s32_nn(prev, b))
+        prev = got
+
+
 def test_f16_8192_sweep_identical_across_stages():
     wl = inputs.WORKLOADS["f16_nt_8192"]
     a, b = wl.lhs(), wl.rhs()
