@@ -24,6 +24,7 @@ Prints ONE JSON line (rank 0):
                            ragged 4000x3000x2050 S=3 and the 8192^3 S=1..6 sweep,
                            and 16 independent 1024^3 f16 / s32 GEMMs issued
                            on 1, 2, 4 or 8 streams (host concurrency)
+                           and per-launch median / p10 / p90 at 4096^3, 8192^3
 
 --impl reference times the CPU oracle instead (the slow reference arm).
 With torchrun (N > 1) every rank runs an independent replica of the workload
@@ -283,6 +284,32 @@ def e2e_pipelined(pws, torch, dev, a_h, b_h, c_h, stages, n_steps, warmup=2):
     return e0.elapsed_time(e1) / n_steps
 
 
+def per_launch_distribution(pws, torch, stream, shapes=((4096, 4), (8192, 4)), n=60, warmup=10):
+    """Each of n back-to-back launches timed by its own pair of CUDA events on
+    the launching stream (after `warmup` untimed ones): median, p10 and p90."""
+    out = {}
+    dev = torch.device("cuda")
+    for M, S in shapes:
+        a = torch.rand(M, M, device=dev, dtype=torch.float16) * 2 - 1
+        b = torch.rand(M, M, device=dev, dtype=torch.float16) * 2 - 1
+        c = torch.empty(M, M, device=dev, dtype=torch.float16)
+        for _ in range(warmup):
+            pws.gemm_f16_nt(a, b, c, stages=S, stream=stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        ev[0].record(stream)
+        for i in range(n):
+            pws.gemm_f16_nt(a, b, c, stages=S, stream=stream)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        us = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(n))
+        pick = lambda q: us[min(n - 1, int(q * n))]
+        out[f"f16_nt_{M}^3/S{S}/per_launch"] = {
+            "median_us": round(pick(0.5), 1), "p10_us": round(pick(0.1), 1), "p90_us": round(pick(0.9), 1),
+            "median_TFLOP_s": round(2 * M ** 3 / pick(0.5) / 1e6, 1), "launches": n}
+        del a, b, c
+    return out
+
+
 def concurrency_configs(pws, torch, G=16, stream_counts=(1, 2, 4, 8)):
     """Host concurrency: G independent GEMMs of one small shape, issued
     round-robin on n streams (fork from one stream, join back), captured in a
@@ -370,6 +397,7 @@ def extra_configs(pws, torch, stream, reps=20):
             out[name + ("/" + suffix if suffix else "")] = res
         del a, b, c
     out.update(concurrency_configs(pws, torch))
+    out.update(per_launch_distribution(pws, torch, stream))
     return out
 
 
