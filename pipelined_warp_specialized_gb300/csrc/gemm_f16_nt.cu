@@ -846,6 +846,8 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 // Fills a f16 [M,N] output with zeros (K == 0: the empty sum).
 __global__ void zero_fill_u16(unsigned short* out, int64_t n) {
+    grid_dependency_wait();             // launched as a programmatic dependent
+    allow_dependent_launch();
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
         out[i] = 0;
@@ -860,6 +862,10 @@ __global__ void zero_fill_u16(unsigned short* out, int64_t n) {
 __global__ void __launch_bounds__(256)
 repack_rows_kernel(const uint16_t* __restrict__ a, int64_t ma, const uint16_t* __restrict__ b, int64_t nb, int K,
                    int Kp, uint16_t* __restrict__ dst_a, uint16_t* __restrict__ dst_b, int pairs) {
+    // launched as a programmatic dependent; the GEMM that follows may start
+    // its set-up while the copy finishes
+    grid_dependency_wait();
+    allow_dependent_launch();
     const int64_t chunks = Kp / 8;
     const int64_t total = (ma + nb) * chunks;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -1149,8 +1155,10 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
         const int64_t n = M * N;
         int blocks = static_cast<int>((n + 255) / 256);
         if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
-        zero_fill_u16<<<blocks, 256, 0, stream>>>(reinterpret_cast<unsigned short*>(out), n);
-        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+        return launch_pdl(zero_fill_u16, dim3(blocks), dim3(256), 0, stream, reinterpret_cast<unsigned short*>(out), n) ==
+                       cudaSuccess
+                   ? GEMM_OK
+                   : GEMM_ERR_LAUNCH;
     }
     const unsigned flags = debug_flags();
     Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
@@ -1174,9 +1182,8 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
                               reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
             const int64_t total = (M + N) * (Kp / 8);
             const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
-            repack_rows_kernel<<<blocks, 256, 0, stream>>>(lhs, M, rhs, N, static_cast<int>(K), static_cast<int>(Kp),
-                                                           da, db, pairs);
-            if (cudaGetLastError() != cudaSuccess) {
+            if (launch_pdl(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, lhs, M, rhs, N, static_cast<int>(K),
+                           static_cast<int>(Kp), da, db, pairs) != cudaSuccess) {
                 scratch_free(scratch, stream);
                 return GEMM_ERR_LAUNCH;
             }
@@ -1306,8 +1313,10 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
         const int64_t n = M * N;
         int blocks = static_cast<int>((n + 255) / 256);
         if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
-        zero_fill_u16<<<blocks, 256, 0, stream>>>(reinterpret_cast<unsigned short*>(out), n);
-        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+        return launch_pdl(zero_fill_u16, dim3(blocks), dim3(256), 0, stream, reinterpret_cast<unsigned short*>(out), n) ==
+                       cudaSuccess
+                   ? GEMM_OK
+                   : GEMM_ERR_LAUNCH;
     }
     const unsigned flags = debug_flags();
     const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
@@ -1329,9 +1338,9 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
                           reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
         const int64_t total = (M + N) * (Kp / 8);
         const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
-        repack_rows_kernel<<<blocks, 256, 0, stream>>>(lhs, M, rhs, N, static_cast<int>(K), static_cast<int>(Kp), da,
-                                                       db, pairs);
-        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+        if (launch_pdl(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, lhs, M, rhs, N, static_cast<int>(K),
+                       static_cast<int>(Kp), da, db, pairs) != cudaSuccess)
+            return GEMM_ERR_LAUNCH;
         a_src = da;
         b_src = db;
         ld = Kp;
