@@ -26,10 +26,12 @@ def gpu():
     pws.gemm_set_wait_timeout_ns(0)
 
 
-@pytest.mark.parametrize("extra", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER],
-                         ids=["solo_tma", "pair_tma", "solo_copy"])
-def test_missing_seed_times_out_and_context_survives(extra):
-    M, N, K = 256, 256, 256
+@pytest.mark.parametrize("extra,N", [
+    (0, 256), (pws.GEMM_DEBUG_FORCE_PAIR_TILE, 256), (pws.GEMM_DEBUG_FORCE_COPY_PRODUCER, 256),
+    (pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE, 512),   # split accumulator, 8 epilogue warps
+], ids=["solo_tma", "pair_tma", "solo_copy", "wide_tma"])
+def test_missing_seed_times_out_and_context_survives(extra, N):
+    M, K = 256, 256
     a_np = inputs.uniform_f16(2, 0, (M, K))
     b_np = inputs.uniform_f16(2, 1, (N, K))
     a = torch.from_numpy(a_np).cuda()
