@@ -25,6 +25,14 @@
  *   - Calls are asynchronous and stream-ordered on `stream` (0 = the legacy
  *     default stream).  They do not synchronize and do not allocate device
  *     memory per call.
+ *   - Kernels are launched with programmatic stream serialization: a call's
+ *     kernel may be scheduled while the previous kernel on the stream is
+ *     still running, but it reads and writes global memory only after that
+ *     kernel has completed, so stream order holds for every memory effect.
+ *     It also lets the next kernel on the stream be scheduled early; a
+ *     caller's own kernel launched with that attribute after a call must
+ *     execute griddepcontrol.wait (cudaGridDependencySynchronize) before
+ *     reading the call's output, as that attribute always requires.
  *   - Argument errors are reported by the return value BEFORE any launch;
  *     nothing is written in that case.
  *   - M == 0 or N == 0 is a successful no-op.  K == 0 writes zeros to `out`
