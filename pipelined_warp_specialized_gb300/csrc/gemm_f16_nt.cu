@@ -24,27 +24,35 @@
 //   * consumer  -- one warp (one elected thread) seeds every empty[s] once
 //                  before its loop ("foreach {s} in [MATMUL_STAGES] trigger
 //                  empty[s]"), then per K block waits full[s], issues four
-//                  tcgen05.mma (K = 16 each) into an fp32 accumulator in
-//                  tensor memory, and commits to empty[s] -- the commit is
+//                  tcgen05.mma (K = 16 each; eight for the wide tile) into an
+//                  fp32 accumulator in tensor memory, and commits to
+//                  empty[s] -- the commit is
 //                  the "mma.commit" fence: the slot is released only once the
 //                  multiplies reading it have completed.
-//   * epilogue  -- four warps, one per 32-lane quarter of tensor memory,
-//                  wait for the accumulator, read it with tcgen05.ld, round to
-//                  f16 (nearest even), stage 32 x 64 blocks in swizzled shared
+//   * epilogue  -- four warps, one per 32-lane quarter of tensor memory
+//                  (eight, two per quarter, for the wide tile), wait for the
+//                  accumulator, read it with tcgen05.ld, round to f16
+//                  (nearest even), stage 32 x 64 blocks in swizzled shared
 //                  memory and store them with TMA (clipped at M and N), or
 //                  with guarded plain stores where TMA cannot address `out`.
 //
 // The kernel is persistent (the Croqtile tutorial ch.5 "持久调度与 if 守卫"):
-// a fixed grid strides over output tiles, and the accumulator is double
-// buffered in tensor memory so the epilogue of tile i overlaps the main loop
-// of tile i+1 (two more event pairs, tmem_full[2] / tmem_empty[2], seeded by
-// the epilogue warps the same way).
+// a fixed grid strides over work units (output tiles, or half tiles in a
+// partial last wave), and the accumulator is double buffered in tensor memory
+// so the epilogue of unit i overlaps the main loop of unit i+1 (two more
+// event pairs, tmem_full[2] / tmem_empty[2], seeded by the epilogue warps the
+// same way).
 //
-// Two tile shapes share the code: a CTA pair (cta_group::2, 256 x 256 per
-// pair, each CTA loading its own 128 rows of A and 128 rows of B -- no
-// multicast) and a single CTA (128 x 128).  Every ring slot is 32 KB per CTA
-// in both, so S = 1..6 fit the shared memory with the epilogue staging, and
-// for a fixed shape the tile configuration does not depend on S.
+// Three tile shapes share the code.  A CTA pair (cta_group::2) computes
+// 256 x 256 (each CTA loading its own 128 rows of A and 128 rows of B -- no
+// multicast), or, for rings of up to four slots, 256 x 512 with two B boxes
+// per slot and one 512-column accumulator drained in two halves; a single CTA
+// computes 128 x 128.  The tile is chosen from the shape and S alone, and
+// every tile sums each output element over K in the same order.
+//
+// Grids are launched as programmatic dependents: set-up (barriers, tensor
+// memory, cluster) overlaps the previous grid on the stream, and global
+// memory is touched only once that grid has completed.
 //
 // Every wait is bounded (wait_timeout_ns); a role that gives up records a
 // timeout in the library's status word, raises a CTA-local abort flag that
