@@ -545,14 +545,14 @@ def run_reference(args, world, rank):
     import oracle
     M, N, K = args.M, args.N, args.K
     threads = oracle.default_threads()
-    b = inputs.uniform_f16(5, 1, (N, K))
-    a_probe = inputs.uniform_f16(5, 0, (max(1, threads), K))
+    b = args.wl.rhs()
+    a_probe = args.wl.lhs_rows(max(1, min(M, threads)))
     # size one step so the whole warm-up + timed run stays within ~90 s
     t = oracle_time(a_probe, b, max(1, threads))
     per_row = t / max(1, threads)
     budget = 90.0 / max(1, args.steps + args.warmup)
     rows = int(max(1, min(M, budget / max(per_row, 1e-6))))
-    a = inputs.uniform_f16(5, 0, (rows, K))
+    a = args.wl.lhs_rows(rows)
     for _ in range(args.warmup):
         oracle.gemm_f16_nt_f64(a, b)
     t0 = time.perf_counter()
@@ -566,7 +566,10 @@ def run_reference(args, world, rank):
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"f16_nt_{M}x{N}x{K}", "M": M, "N": N, "K": K, "sample_rows": rows},
+        "config": {"workload": args.wl.name, "M": M, "N": N, "K": K, "stages": args.stages,
+                   "accumulate": "f64 (the oracle)", "layout": "lhs[M,K] rhs[N,K] out[M,N] row-major",
+                   "values": f"{args.wl.dist} (seed {args.wl.seed}) rounded to f16",
+                   "parallelism": "host cores", "sample_rows": rows},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

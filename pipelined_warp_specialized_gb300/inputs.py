@@ -115,6 +115,13 @@ class Workload:
             return ints(self.seed, 0, (self.M, self.K))
         return _f16(self.dist, self.seed, 0, (self.M, self.K))
 
+    def lhs_rows(self, rows: int) -> np.ndarray:
+        """The first `rows` rows of lhs() (the generator is counter-based in
+        row-major element order, so they need not generate the rest)."""
+        if self.kind == "s32_nn":
+            return ints(self.seed, 0, (rows, self.K))
+        return _f16(self.dist, self.seed, 0, (rows, self.K))
+
     def rhs(self) -> np.ndarray:
         if self.kind == "s32_nn":
             return ints(self.seed, 1, (self.K, self.N))
