@@ -247,6 +247,31 @@ def test_f16_wide_tile_tail_split(M, N, K):
     assert_f16_ok(split, oracle.gemm_f16_nt_f64(a, b), K)
 
 
+@pytest.mark.parametrize("stages,flags", [
+    (4, pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE),
+    (6, pws.GEMM_DEBUG_FORCE_PAIR_TILE),
+    (2, pws.GEMM_DEBUG_FORCE_SOLO_TILE),
+], ids=["wide", "pair", "solo"])
+def test_f16_long_k(stages, flags):
+    # 1025 K blocks, the last one ragged: the ring laps each slot hundreds of
+    # times, so every event's phase flips hundreds of times within one unit
+    M, N, K = 300, 520, 65536 + 40
+    a = inputs.uniform_f16(95, 0, (M, K))
+    b = inputs.uniform_f16(95, 1, (N, K))
+    assert_f16_ok(run_f16(a, b, stages, flags), oracle.gemm_f16_nt_f64(a, b), K)
+
+
+@pytest.mark.parametrize("M,N,K,stages", [
+    (131072 + 77, 64, 64, 6),        # 513 pair tile rows: 65 raster groups of 8
+    (131072 + 77, 512, 72, 4),       # the same with the wide tile
+    (64, 131072 + 296, 64, 4),       # 257 wide tile columns (the last one ragged), walked both ways
+])
+def test_f16_very_tall_and_very_wide(M, N, K, stages):
+    a = inputs.normal_f16(96, 0, (M, K))
+    b = inputs.normal_f16(96, 1, (N, K))
+    assert_f16_ok(run_f16(a, b, stages), oracle.gemm_f16_nt_f64(a, b), K)
+
+
 def test_f16_k_zero_and_empty():
     a = np.zeros((7, 0), np.float16)
     b = np.zeros((5, 0), np.float16)
