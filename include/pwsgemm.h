@@ -229,6 +229,11 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *       its 256x256 tile, never the wide 256x512 one.
  *   GEMM_DEBUG_FORCE_WIDE_TILE     : where the CTA pair is used and stages is
  *       at most 4, always use the wide 256x512 tile.
+ *   GEMM_DEBUG_SKIP_ACC_SEED       : the epilogue does not seed the
+ *       accumulator's empty events, so the multiply role's first wait for
+ *       the accumulator never completes while the producer has already
+ *       filled the ring; used to test that this deadlock, with copies
+ *       issued, also ends in GEMM_ERR_TIMEOUT and a clean exit.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -239,7 +244,8 @@ enum {
     GEMM_DEBUG_FORCE_PAIR_TILE = 16u,
     GEMM_DEBUG_NO_SPLIT = 32u,
     GEMM_DEBUG_FORCE_NARROW_TILE = 64u,
-    GEMM_DEBUG_FORCE_WIDE_TILE = 128u
+    GEMM_DEBUG_FORCE_WIDE_TILE = 128u,
+    GEMM_DEBUG_SKIP_ACC_SEED = 256u
 };
 int gemm_set_debug_flags(unsigned flags);
 

@@ -37,6 +37,7 @@ GEMM_DEBUG_FORCE_PAIR_TILE = 16
 GEMM_DEBUG_NO_SPLIT = 32
 GEMM_DEBUG_FORCE_NARROW_TILE = 64
 GEMM_DEBUG_FORCE_WIDE_TILE = 128
+GEMM_DEBUG_SKIP_ACC_SEED = 256
 
 _lib = None
 

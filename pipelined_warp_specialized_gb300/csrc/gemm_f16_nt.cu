@@ -469,6 +469,14 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
                     for (uint32_t it = first; it < issued; ++it)
                         if (!Dn.wait(bFULL + 8 * (it % S), (it / S) & 1u)) break;
+                } else if (!ok && issued > 0) {
+                    // A pair's peer: its copies signal the leader's barriers,
+                    // which it cannot wait on, and the leader may have given
+                    // up before arming them.  A copy lands within microseconds;
+                    // waiting 1 ms (bounded) before the exit path keeps any
+                    // still in flight from landing after the CTA is gone.
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
                 }
             }
         } else if constexpr (CG == 1) {
@@ -693,7 +701,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const uint32_t tempty_leader = (CG == 2) ? mapa_shared(bTEMPTY, 0) : bTEMPTY;
         // seed: both accumulator event pairs start free (the two buffers of
         // the 256 x 256 and 128 x 128 tiles, the two halves of the wide one)
-        if (lane == 0) {
+        if (lane == 0 && !(p.flags & GEMM_DEBUG_SKIP_ACC_SEED)) {
             for (int b = 0; b < 2; ++b) {
                 if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * b);
                 else mbar_arrive_cluster(tempty_leader + 8 * b);

@@ -26,11 +26,18 @@ def gpu():
     pws.gemm_set_wait_timeout_ns(0)
 
 
+@pytest.mark.parametrize("seed_flag", [pws.GEMM_DEBUG_SKIP_EMPTY_SEED, pws.GEMM_DEBUG_SKIP_ACC_SEED],
+                         ids=["no_empty_seed", "no_acc_seed"])
 @pytest.mark.parametrize("extra,N", [
     (0, 256), (pws.GEMM_DEBUG_FORCE_PAIR_TILE, 256), (pws.GEMM_DEBUG_FORCE_COPY_PRODUCER, 256),
     (pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE, 512),   # split accumulator, 8 epilogue warps
 ], ids=["solo_tma", "pair_tma", "solo_copy", "wide_tma"])
-def test_missing_seed_times_out_and_context_survives(extra, N):
+def test_missing_seed_times_out_and_context_survives(seed_flag, extra, N):
+    # Without the empty seed the producer's first wait never completes: no
+    # copy is ever issued.  Without the accumulator seed the multiply role's
+    # first wait never completes while the producer has filled both slots
+    # (K = 256 is four K blocks, S = 2): the roles give up with copies
+    # issued, and a pair's producers drain them before the CTAs exit.
     M, K = 256, 256
     a_np = inputs.uniform_f16(2, 0, (M, K))
     b_np = inputs.uniform_f16(2, 1, (N, K))
@@ -38,7 +45,7 @@ def test_missing_seed_times_out_and_context_survives(extra, N):
     b = torch.from_numpy(b_np).cuda()
     assert pws.gemm_device_status() == pws.GEMM_OK          # clear anything earlier
     pws.gemm_set_wait_timeout_ns(200_000_000)               # 0.2 s per wait
-    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_SKIP_EMPTY_SEED | extra)
+    pws.gemm_set_debug_flags(seed_flag | extra)
     try:
         pws.gemm_f16_nt(a, b, stages=2)
         torch.cuda.synchronize()                             # the kernel returns by itself
