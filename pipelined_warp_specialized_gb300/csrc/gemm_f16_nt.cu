@@ -79,7 +79,6 @@ constexpr int BM_CTA = 128;            // A rows per CTA (tensor-memory lanes)
 constexpr int BN_CTA = 128;            // B rows per CTA
 constexpr int A_SLOT = BM_CTA * BK * 2;
 constexpr int B_SLOT = BN_CTA * BK * 2;
-constexpr int SLOT_BYTES = A_SLOT + B_SLOT;   // 32 KB
 constexpr int EPI_WARPS = 4;           // epilogue warps: one per tensor-memory lane quarter, two staging buffers each
 constexpr int EPI_WARPS_WIDE = 8;      // the wide tile's: two per lane quarter, one staging buffer each
 constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128 bytes of f16)
