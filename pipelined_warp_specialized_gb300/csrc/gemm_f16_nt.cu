@@ -114,7 +114,8 @@ struct Params {
     // Work units: units 0 .. full_units-1 are whole output tiles (unit = tile).
     // With split == 2, each remaining tile (those of the last, partial wave)
     // is cut into two units, its left and right halves of columns, which run
-    // the full K loop with a half-width MMA (no partial sums to combine).
+    // the full K loop (no partial sums to combine): with a half-width MMA, or
+    // for the wide tile with one of its two MMAs.
     int full_units;
     int split;
     int total_units;
