@@ -197,22 +197,11 @@ extern "C" int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, 
 namespace pws {
 namespace s32nn {
 
-// cp.async.wait_group with a run-time count (the instruction takes an immediate).
-__device__ __forceinline__ void cp_async_wait_upto(int pending) {
-    switch (pending) {
-        case 0: cp_async_wait_group<0>(); break;
-        case 1: cp_async_wait_group<1>(); break;
-        case 2: cp_async_wait_group<2>(); break;
-        case 3: cp_async_wait_group<3>(); break;
-        case 4: cp_async_wait_group<4>(); break;
-        default: cp_async_wait_group<5>(); break;
-    }
-}
-
-template <int BM, int BN, int TM, int TN, int CBYTES>
+template <int BM, int BN, int TM, int TN, int CBYTES, int S>
 __global__ void __launch_bounds__(THREADS)
-gemm_s32_nn_ring_kernel(int M, int N, int K, int S, const int32_t* __restrict__ lhs,
-                        const int32_t* __restrict__ rhs, int32_t* __restrict__ out) {
+gemm_s32_nn_ring_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, const int32_t* __restrict__ rhs,
+                        int32_t* __restrict__ out) {
+    static_assert(S >= 2 && S <= 6, "ring slots");
     static_assert((BM / TM) * (BN / TN) == THREADS, "one thread per TM x TN block");
     constexpr int A_WORDS = BM * (BK + APAD);      // one slot of A: [BM][BK + APAD]
     constexpr int B_WORDS = BK * BN;               // one slot of B: [BK][BN]
@@ -260,14 +249,20 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, int S, const int32_t* __restrict__ 
         if (t < T) issue(t, t);
         cp_async_commit();
     }
+    // The slot names rotate by one per iteration (the page's rotate): tile t
+    // is read from slot `cur`, tile t + S - 1 is loaded into slot `nxt`, the
+    // one tile t - 1 vacated.  With S a run-time value, computing t mod S
+    // made the loop execute 60 % more instructions and take twice the cycles
+    // on GB300; with S fixed at compile time and the names incremented, the
+    // loop is the two-buffer kernel's plus the extra slots in flight.
+    int cur = 0, nxt = S - 1;
     for (int t = 0; t < T; ++t) {
-        const int nt = t + S - 1;
-        if (nt < T) issue(nt, nt % S);       // the slot tile t - 1 vacated
+        if (t + S - 1 < T) issue(t + S - 1, nxt);
         cp_async_commit();
-        cp_async_wait_upto(S - 1);           // tile t has landed ...
+        cp_async_wait_group<S - 1>();        // tile t has landed ...
         __syncthreads();                     // ... and is visible to all threads
-        const int32_t* a = As + (t % S) * A_WORDS;
-        const int32_t* b = Bs + (t % S) * B_WORDS;
+        const int32_t* a = As + cur * A_WORDS;
+        const int32_t* b = Bs + cur * B_WORDS;
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             uint32_t av[TM], bv[TN];
@@ -280,7 +275,9 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, int S, const int32_t* __restrict__ 
 #pragma unroll
                 for (int j = 0; j < TN; ++j) acc[i][j] += av[i] * bv[j];
         }
-        __syncthreads();                     // slot t mod S is free for tile t + S
+        __syncthreads();                     // slot `cur` is free for tile t + S
+        cur = cur + 1 == S ? 0 : cur + 1;
+        nxt = nxt + 1 == S ? 0 : nxt + 1;
     }
     cp_async_wait_group<0>();
 
@@ -296,29 +293,39 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, int S, const int32_t* __restrict__ 
     }
 }
 
+template <int BM, int BN, int TM, int TN, int CBYTES, int S>
+cudaError_t launch_ring_s(int M, int N, int K, const int32_t* lhs, const int32_t* rhs, int32_t* out, int device,
+                          cudaStream_t stream) {
+    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+    constexpr size_t smem = static_cast<size_t>(S) * (BM * (BK + APAD) + BK * BN) * sizeof(int32_t);
+    auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, CBYTES, S>;
+    static bool configured[64] = {};
+    if (smem > 48 * 1024 && !configured[device]) {      // above the default dynamic limit: opt in once
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+            return cudaGetLastError();
+        configured[device] = true;
+    }
+    return launch_pdl(k, grid, dim3(THREADS), smem, stream, M, N, K, lhs, rhs, out);
+}
+
+template <int BM, int BN, int TM, int TN, int CBYTES>
+cudaError_t launch_ring_c(int M, int N, int K, int S, const int32_t* lhs, const int32_t* rhs, int32_t* out, int device,
+                          cudaStream_t stream) {
+    switch (S) {
+        case 2: return launch_ring_s<BM, BN, TM, TN, CBYTES, 2>(M, N, K, lhs, rhs, out, device, stream);
+        case 3: return launch_ring_s<BM, BN, TM, TN, CBYTES, 3>(M, N, K, lhs, rhs, out, device, stream);
+        case 4: return launch_ring_s<BM, BN, TM, TN, CBYTES, 4>(M, N, K, lhs, rhs, out, device, stream);
+        case 5: return launch_ring_s<BM, BN, TM, TN, CBYTES, 5>(M, N, K, lhs, rhs, out, device, stream);
+        case 6: return launch_ring_s<BM, BN, TM, TN, CBYTES, 6>(M, N, K, lhs, rhs, out, device, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <int BM, int BN, int TM, int TN>
 cudaError_t launch_ring(int M, int N, int K, int S, const int32_t* lhs, const int32_t* rhs, int32_t* out,
                         bool vec16, int device, cudaStream_t stream) {
-    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-    const size_t smem = static_cast<size_t>(S) * (BM * (BK + APAD) + BK * BN) * sizeof(int32_t);
-    static bool configured16[64] = {}, configured4[64] = {};
-    if (vec16) {
-        auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, 16>;
-        if (!configured16[device]) {
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 6 * (BM * (BK + APAD) + BK * BN) * 4) != cudaSuccess)
-                return cudaGetLastError();
-            configured16[device] = true;
-        }
-        return launch_pdl(k, grid, dim3(THREADS), smem, stream, M, N, K, S, lhs, rhs, out);
-    } else {
-        auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, 4>;
-        if (!configured4[device]) {
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 6 * (BM * (BK + APAD) + BK * BN) * 4) != cudaSuccess)
-                return cudaGetLastError();
-            configured4[device] = true;
-        }
-        return launch_pdl(k, grid, dim3(THREADS), smem, stream, M, N, K, S, lhs, rhs, out);
-    }
+    return vec16 ? launch_ring_c<BM, BN, TM, TN, 16>(M, N, K, S, lhs, rhs, out, device, stream)
+                 : launch_ring_c<BM, BN, TM, TN, 4>(M, N, K, S, lhs, rhs, out, device, stream);
 }
 
 }  // namespace s32nn
