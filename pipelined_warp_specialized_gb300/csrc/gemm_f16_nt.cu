@@ -60,6 +60,7 @@
 // the kernel always returns.
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -1036,16 +1037,18 @@ int capacity(const DeviceInfo& info, int threads) {
     auto kern = gemm_f16_nt_kernel<CG, S, NW>;
     constexpr int smem = Layout<S, NW>::DYN;
     static_assert(Layout<S, NW>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
-    static int configured[64] = {};
-    static int max_clusters[64] = {};
-    if (!configured[info.device]) {
+    // per-device caches; concurrent first calls from several host threads
+    // compute and store the same values
+    static std::atomic<int> configured[64] = {};
+    static std::atomic<int> max_clusters[64] = {};
+    if (!configured[info.device].load(std::memory_order_relaxed)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
-        configured[info.device] = 1;
+        configured[info.device].store(1, std::memory_order_relaxed);
     }
     if constexpr (CG == 1) {
         return info.num_sms;
     } else {
-        if (!max_clusters[info.device]) {
+        if (!max_clusters[info.device].load(std::memory_order_relaxed)) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1062,9 +1065,9 @@ int capacity(const DeviceInfo& info, int threads) {
                 cudaGetLastError();
                 n = info.num_sms / 2;
             }
-            max_clusters[info.device] = n;
+            max_clusters[info.device].store(n, std::memory_order_relaxed);
         }
-        return max_clusters[info.device];
+        return max_clusters[info.device].load(std::memory_order_relaxed);
     }
 }
 

@@ -14,6 +14,7 @@
 //
 // Each thread owns a TM x TN block of outputs held in registers and does
 // TM*TN wrapping 32-bit multiply-adds per K step (IMAD).
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -299,11 +300,11 @@ cudaError_t launch_ring_s(int M, int N, int K, const int32_t* lhs, const int32_t
     const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
     constexpr size_t smem = static_cast<size_t>(S) * (BM * (BK + APAD) + BK * BN) * sizeof(int32_t);
     auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, CBYTES, S>;
-    static bool configured[64] = {};
-    if (smem > 48 * 1024 && !configured[device]) {      // above the default dynamic limit: opt in once
+    static std::atomic<bool> configured[64] = {};       // concurrent first calls store the same value
+    if (smem > 48 * 1024 && !configured[device].load(std::memory_order_relaxed)) {   // above the default limit: opt in once
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
             return cudaGetLastError();
-        configured[device] = true;
+        configured[device].store(true, std::memory_order_relaxed);
     }
     return launch_pdl(k, grid, dim3(THREADS), smem, stream, M, N, K, lhs, rhs, out);
 }

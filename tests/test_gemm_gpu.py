@@ -486,6 +486,43 @@ def test_dependent_s32_chain_reads_completed_outputs():
         prev = got
 
 
+def test_calls_from_concurrent_host_threads():
+    # four host threads call the library at the same time (ctypes releases the
+    # GIL), each on its own stream with a different tile and S, five calls each
+    import threading
+    cases = []
+    for i, (M, N, K, S) in enumerate([(700, 1100, 320, 4), (1024, 1024, 256, 2), (300, 260, 200, 6),
+                                      (2304, 2560, 128, 3)]):
+        a = inputs.uniform_f16(100 + i, 0, (M, K))
+        b = inputs.uniform_f16(100 + i, 1, (N, K))
+        cases.append((_dev(a), _dev(b), oracle.gemm_f16_nt_f64(a, b), K, S))
+    results, errors = [None] * len(cases), []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            da, db, _, _, S = cases[i]
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.default_stream())
+            outs = [pws.gemm_f16_nt(da, db, stages=S, stream=st) for _ in range(5)]
+            st.synchronize()
+            results[i] = outs
+        except Exception as e:          # reported below, in the test's own thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    for (_, _, ref, K, _), outs in zip(cases, results):
+        for o in outs:
+            assert_f16_ok(o.cpu().numpy(), ref, K)
+
+
 def test_f16_8192_sweep_identical_across_stages():
     wl = inputs.WORKLOADS["f16_nt_8192"]
     a, b = wl.lhs(), wl.rhs()
