@@ -202,6 +202,21 @@ def time_launches(fn, steps, warmup, torch, stream):
     return e0.elapsed_time(e1) / steps
 
 
+def time_steady(fn, torch, stream, warm_s=0.25, timed_s=0.25):
+    """Average ms per launch of fn() once the board has settled.
+
+    The launch count is sized from a short probe so that every point of a
+    sweep gets the same warm-up time and the same timed time: under the
+    board's power limit the clock a launch sees depends on the load of the
+    preceding fraction of a second, so equal launch COUNTS would hand later
+    points the power state earlier ones left behind.
+    """
+    probe = time_launches(fn, 5, 3, torch, stream)
+    warm = max(3, int(warm_s / (probe * 1e-3)))
+    steps = max(5, int(timed_s / (probe * 1e-3)))
+    return time_launches(fn, steps, warm, torch, stream)
+
+
 def time_graph(fn, torch, per_graph=20, replays=20):
     """Average ms per launch of fn(stream), replayed from a CUDA graph.
 
@@ -344,7 +359,7 @@ def concurrency_configs(pws, torch, G=16, stream_counts=(1, 2, 4, 8)):
     return out
 
 
-def extra_configs(pws, torch, stream, reps=20):
+def extra_configs(pws, torch, stream):
     """Kernel-only timings of every workload (inputs resident)."""
     out = {}
     dev = torch.device("cuda")
@@ -378,20 +393,18 @@ def extra_configs(pws, torch, stream, reps=20):
                 plan = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), wl.stages[0])
                 label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B", 2: "repack+tma"}[plan["producer"]]
                 res = {"producer": label, "cta_group": plan["cta_group"]}
-                n = reps if wl.M * wl.N * wl.K < 2 ** 36 else max(5, reps // 2)
                 small = wl.flops < 2 ** 34        # launch-bound: time from a CUDA graph
                 for s in wl.stages:
                     if small and not plan["producer"] == 2:
                         ms = time_graph(lambda st: pws.gemm_f16_nt(a, b, c, stages=s, stream=st), torch)
                     else:
-                        ms = time_launches(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), n * 5, 3,
-                                           torch, stream)
+                        ms = time_steady(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), torch, stream)
                     ps = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), s)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
                                     "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1),
                                     "tile": f"{ps['bm']}x{ps['bn']}"}
-                    if small and not plan["producer"] == 2:
-                        res[f"S{s}"]["timing"] = "CUDA-graph replay"
+                    res[f"S{s}"]["timing"] = ("CUDA-graph replay" if small and not plan["producer"] == 2
+                                              else "0.25 s warm-up, then 0.25 s of back-to-back launches")
             finally:
                 pws.gemm_set_debug_flags(0)
             out[name + ("/" + suffix if suffix else "")] = res
