@@ -125,9 +125,11 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  * The producer uses the tensor memory accelerator (TMA) when both operands
  * start on 16-byte boundaries and K is a multiple of 8 (row stride a multiple
  * of 16 bytes).  Otherwise the call first copies both operands into rows of
- * ceil(K/8)*8 elements in scratch memory taken, stream-ordered, from a memory
- * pool the library owns on the current device ((M+N)*ceil(K/8)*16 bytes,
- * returned to the pool on `stream` after the GEMM; the pool keeps freed
+ * ceil(K/64)*64 elements (128-byte aligned rows, which the accelerator reads
+ * faster than rows at other multiples of 16 bytes) in scratch memory taken,
+ * stream-ordered, from a memory pool the library owns on the current device
+ * (about (M+N)*ceil(K/64)*128 bytes, each operand's part rounded up to 256
+ * bytes, returned to the pool on `stream` after the GEMM; the pool keeps freed
  * memory for the next call, so repeated calls of one size request no new
  * memory and never synchronize).  If the pool cannot supply it, an
  * asynchronous-copy producer fills the same swizzled ring straight from the
@@ -142,6 +144,16 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  * feeds 4/3 as many flops (5 and 6 slots of that size do not fit in shared
  * memory).  Every tile sums each output element over K in the same order,
  * so the tile choice never changes the result.
+ *
+ * K split: when the 128 x 128 tile is used, the tiles fill at most half of
+ * the SMs and K spans at least 32 blocks of 64 (K > 1984), each tile is
+ * computed by a cluster of two CTAs.  One sums the first ceil(nkb/2) K
+ * blocks, the other the rest (nkb = ceil(K/64)), each into its own fp32
+ * accumulator.  The two partial sums are added (one fp32 addition) before
+ * the rounding to f16.  Such an output is therefore
+ * f16(sum over the first half + sum over the second half), a different
+ * rounding of the same exact sum than the one-pass tiles give.  The choice
+ * depends on M, N and K only, so the result is still the same for every S.
  *
  * The kernel is persistent: a grid of as many CTA groups as fit on the GPU
  * strides over the output tiles.  When the tile count leaves a last, partial
@@ -234,6 +246,12 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *       the accumulator never completes while the producer has already
  *       filled the ring; used to test that this deadlock, with copies
  *       issued, also ends in GEMM_ERR_TIMEOUT and a clean exit.
+ *   GEMM_DEBUG_NO_KSPLIT           : never split K over a cluster of two
+ *       CTAs (gemm_f16_nt does for small outputs, see above); the result is
+ *       then the one-pass sum every other tile gives.
+ *   GEMM_DEBUG_FORCE_KSPLIT        : split K wherever the single-CTA tile is
+ *       used and there are at least 2 K blocks, however many tiles there are
+ *       (clusters beyond those that fit at once run as the GPU frees SMs).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -245,7 +263,9 @@ enum {
     GEMM_DEBUG_NO_SPLIT = 32u,
     GEMM_DEBUG_FORCE_NARROW_TILE = 64u,
     GEMM_DEBUG_FORCE_WIDE_TILE = 128u,
-    GEMM_DEBUG_SKIP_ACC_SEED = 256u
+    GEMM_DEBUG_SKIP_ACC_SEED = 256u,
+    GEMM_DEBUG_NO_KSPLIT = 512u,
+    GEMM_DEBUG_FORCE_KSPLIT = 1024u
 };
 int gemm_set_debug_flags(unsigned flags);
 
@@ -256,12 +276,13 @@ int gemm_set_debug_flags(unsigned flags);
  *   plan[0] tile rows per CTA group (BM)      plan[1] tile columns (BN)
  *   plan[2] K per ring slot (BK)              plan[3] CTAs per tile (1 or 2)
  *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy,
- *           2 = tensor memory accelerator on a 16-byte aligned scratch copy
+ *           2 = tensor memory accelerator on an aligned scratch copy
  *   plan[5] copy granularity in bytes (16 for TMA, else 8, 4 or 2)
  *   plan[6] output store: 0 = tensor memory accelerator, 1 = plain stores
  *   plan[7] dynamic shared memory bytes per CTA
  *   plan[8] number of output tiles        plan[9] number of K blocks
- * `plan` must hold 10 int64 values.
+ *   plan[10] CTAs summing parts of K per tile: 1, or 2 (the K split)
+ * `plan` must hold 11 int64 values.
  */
 int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                      const gemm_f16_t* out, int stages, int64_t* plan);

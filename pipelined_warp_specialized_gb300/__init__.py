@@ -38,6 +38,8 @@ GEMM_DEBUG_NO_SPLIT = 32
 GEMM_DEBUG_FORCE_NARROW_TILE = 64
 GEMM_DEBUG_FORCE_WIDE_TILE = 128
 GEMM_DEBUG_SKIP_ACC_SEED = 256
+GEMM_DEBUG_NO_KSPLIT = 512
+GEMM_DEBUG_FORCE_KSPLIT = 1024
 
 _lib = None
 
@@ -222,9 +224,10 @@ def gemm_f16_nt_plan(M: int, N: int, K: int, lhs_ptr: int = 1 << 40, rhs_ptr: in
                      out_ptr: int = 3 << 40, stages: int = 4) -> dict:
     """The launch plan gemm_f16_nt would use (host logic only; the pointers are
     only inspected for alignment and overlap, never dereferenced)."""
-    plan = (ctypes.c_int64 * 10)()
+    plan = (ctypes.c_int64 * 11)()
     _check(load_library().gemm_f16_nt_plan(M, N, K, lhs_ptr, rhs_ptr, out_ptr, stages, plan), "gemm_f16_nt_plan")
-    keys = ["bm", "bn", "bk", "cta_group", "producer", "copy_bytes", "store", "smem_bytes", "tiles", "k_blocks"]
+    keys = ["bm", "bn", "bk", "cta_group", "producer", "copy_bytes", "store", "smem_bytes", "tiles", "k_blocks",
+            "k_split"]
     return dict(zip(keys, list(plan)))
 
 

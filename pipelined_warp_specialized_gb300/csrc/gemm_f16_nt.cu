@@ -120,6 +120,11 @@ struct Params {
     int full_units;
     int split;
     int total_units;
+    // K split (single-CTA tile only): 2 = each tile is computed by a cluster
+    // of two CTAs, rank r summing its K blocks [kb0(r), kb1(r)) -- the first
+    // ceil(num_kb / 2) blocks, or the rest -- and the two fp32 partial tiles
+    // are added once before rounding.  One tile per cluster, no persistence.
+    int ksplit;
 };
 
 // NW = MMAs per K step, each UMMA_N columns wide.  NW = 1: the accumulator is
@@ -153,7 +158,8 @@ struct Layout {
     static constexpr int TFULL = EMPTY + 8 * S;
     static constexpr int TEMPTY = TFULL + 16;
     static constexpr int DRAIN = TEMPTY + 16;
-    static constexpr int TMEM_SLOT = DRAIN + 8;
+    static constexpr int RECV = DRAIN + 8;                   // K split: a peer warp's partial rows are staged (x2)
+    static constexpr int TMEM_SLOT = RECV + 16;
     static constexpr int ABORT = TMEM_SLOT + 4;
     static constexpr int END = ABORT + 4;
     static constexpr int BYTES = END + 1024;                // + alignment slack
@@ -311,7 +317,7 @@ __device__ __forceinline__ void copy_strip(uint32_t slot, const __half* base, in
 // k - S + GROUP - 1.
 template <int G, int S>
 __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB, uint32_t bFULL,
-                              uint32_t bEMPTY, int cluster_id, int num_clusters, int lane) {
+                              uint32_t bEMPTY, int cluster_id, int num_clusters, int kb0, int kb1, int lane) {
     constexpr int LAG = S - (S >= 6 ? 2 : 1);
     const int t = threadIdx.x;                   // 0 .. COPY_THREADS - 1
     uint32_t stage = 0, phase = 0, issued = 0, signalled = 0;
@@ -320,7 +326,7 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
         const Unit un = unit_of(u, p);
         int tm, tn;
         tile_coords(un.tile, p, tm, tn);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
             bool got = true;
             if (lane == 0) got = W.wait(bEMPTY + 8 * stage, phase);
             got = __shfl_sync(0xffffffffu, got, 0);
@@ -370,12 +376,20 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int P = static_cast<int>(blockDim.x / 32) - 1 - EW;          // producer warps
     const int mma_warp = P;
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const int cluster_id = blockIdx.x / CG;
-    const int num_clusters = gridDim.x / CG;
+    // K split: a cluster of two single CTAs per tile; krank picks the K half
+    const bool kpair = CG == 1 && p.ksplit == 2;
+    const uint32_t krank = kpair ? cluster_ctarank() : 0u;
+    const int csize = (CG == 2 || kpair) ? 2 : 1;
+    const int cluster_id = blockIdx.x / csize;
+    const int num_clusters = gridDim.x / csize;
+    const int kb_mid = (p.num_kb + 1) / 2;
+    const int kb0 = kpair && krank != 0 ? kb_mid : 0;
+    const int kb1 = kpair && krank == 0 ? kb_mid : p.num_kb;
 
     const uint32_t sA = base + L::A, sB = base + L::B, sEPI = base + L::EPI;
     const uint32_t bFULL = base + L::FULL, bEMPTY = base + L::EMPTY;
     const uint32_t bTFULL = base + L::TFULL, bTEMPTY = base + L::TEMPTY, bDRAIN = base + L::DRAIN;
+    const uint32_t bRECV = base + L::RECV;
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L::ABORT);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::TMEM_SLOT);
 
@@ -392,6 +406,8 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             mbar_init(bTEMPTY + 8 * b, EW * CG);
         }
         mbar_init(bDRAIN, 1);
+        // K split: the 32 lanes of the peer's warp for lane quarter 2*krank + j
+        for (int j = 0; j < 2; ++j) mbar_init(bRECV + 8 * j, 32);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -406,7 +422,13 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync();
+    // A pair's peer issues MMAs into this CTA's tensor memory and copies
+    // against its barriers: it must see them set up.  The K split's first
+    // cross-CTA access comes only after the main loop (the epilogue's), so
+    // its threads arrive here and wait later (the epilogue warps before their
+    // loop, the others at tear-down), out of the way of the first loads.
+    if (CG == 2) cluster_sync();
+    else if (kpair) cluster_arrive_release();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // Launched as a programmatic dependent: everything above (barriers, tensor
@@ -443,7 +465,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const CUtensorMap* tb = NW == 1 && halfw ? &tmBh : &tmB;
                     const int nbox = NW == 1 || halfw ? 1 : NW;
                     const uint32_t bytes = NW == 1 && halfw ? A_SLOT + B_SLOT / 2 : A_SLOT + nbox * B_SLOT;
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!W.wait(bEMPTY + 8 * stage, phase)) { ok = false; break; }
                         const uint32_t a_dst = sA + stage * A_SLOT, b_dst = sB + stage * L::B_STRIDE;
                         if constexpr (CG == 1) {
@@ -484,11 +506,11 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             // cp.async producer (single CTA only): COPY_WARPS warps fill the swizzled slot
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
             if (p.copy_bytes == 8)
-                copy_producer<8, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, lane);
+                copy_producer<8, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, kb0, kb1, lane);
             else if (p.copy_bytes == 4)
-                copy_producer<4, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, lane);
+                copy_producer<4, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, kb0, kb1, lane);
             else
-                copy_producer<2, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, lane);
+                copy_producer<2, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, kb0, kb1, lane);
         }
         __syncwarp();
     } else if (warp == mma_warp) {
@@ -522,8 +544,8 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     // ahead, which only the 6-slot ring can afford: measured on
                     // GB300, pairing is 11 % slower at S = 4 and 2 % slower at S = 5.
                     constexpr int GROUP = S >= 6 ? 2 : 1;
-                    for (int kb = 0; kb < p.num_kb; kb += GROUP) {
-                        const int nb = p.num_kb - kb < GROUP ? p.num_kb - kb : GROUP;
+                    for (int kb = kb0; kb < kb1; kb += GROUP) {
+                        const int nb = kb1 - kb < GROUP ? kb1 - kb : GROUP;
                         uint32_t st[GROUP], ph[GROUP];
                         st[0] = stage;
                         ph[0] = phase;
@@ -542,7 +564,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
                             for (int k = 0; k < BK / UMMA_K; ++k) {
                                 // +32 bytes of K per step: +2 in the (address >> 4) field
-                                tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j) != 0 || k != 0);
+                                tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j) != kb0 || k != 0);
                             }
                         }
                         issued_any = true;
@@ -698,6 +720,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         // ======================================================== epilogue
         const int e = warp - P - 1;              // 0 .. EW-1
         const int q = warp & 3;                  // tensor-memory lane quarter of this warp
+        if (kpair) cluster_wait_acquire();       // the peer's barriers are set up
         const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleEpilogue};
         const uint32_t tempty_leader = (CG == 2) ? mapa_shared(bTEMPTY, 0) : bTEMPTY;
         // seed: both accumulator event pairs start free (the two buffers of
@@ -708,9 +731,51 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 else mbar_arrive_cluster(tempty_leader + 8 * b);
             }
         }
-        // Reads 64 accumulator columns (from tensor-memory address taddr) of
-        // this lane's row and rounds them to 32 packed f16 pairs.
-        auto load_chunk = [&](uint32_t taddr, uint32_t(&h)[32]) {
+        // K split.  Lane quarters 2*krank and 2*krank+1 of the tile are this
+        // CTA's to store.  The warps of the other two quarters are senders:
+        // they copy their fp32 partial sums into this CTA's ring (idle once
+        // the accumulator is complete; one tile per CTA) and arrive on the
+        // peer's recv barrier, whose owner warp adds them to its own partial
+        // sums before rounding.  Staged layout, 16 KB per quarter: 16-byte
+        // unit u (fp32 columns 4u..4u+3) of lane l's row at u * 512 + l * 16,
+        // so that one unit of all 32 rows is one contiguous 512-byte block:
+        // conflict-free to write, and a single request for the peer to read
+        // (read from a 512-byte row per lane, the peer's loads measured 3-4x
+        // slower on GB300).
+        const bool sender = kpair && static_cast<uint32_t>(q >> 1) != krank;
+        const uint32_t stage_lane = sA + static_cast<uint32_t>(q & 1) * (32u * 512u) + static_cast<uint32_t>(lane) * 16u;
+        const uint32_t peer_lane = kpair && !sender ? mapa_shared(stage_lane, krank ^ 1u) : 0u;
+        static_assert(SH::ACC_COLS / 4 * 512 <= 32 * 512 || CG == 2, "a staged quarter holds the single tile's 128 fp32 columns");
+        static_assert(2 * 32 * 512 <= A_SLOT + B_SLOT, "two staged quarters fit in the smallest ring");
+        // Reads 64 accumulator columns (chunk c of the columns starting at
+        // tensor-memory address tbase) of this lane's row, adds the peer's
+        // partial sums of the same columns (K split), and rounds them to 32
+        // packed f16 pairs.
+        auto load_chunk = [&](uint32_t tbase, int c, uint32_t(&h)[32]) {
+            const uint32_t taddr = tbase + static_cast<uint32_t>(c * EPI_COLS);
+            if (peer_lane) {
+                // 32 columns at a time: own partial sums from tensor memory and
+                // the peer's (units 16c + 8 half ..+7) in flight together, then
+                // own + peer, one fp32 add per element (commutative, so the
+                // same bits whichever K half is this CTA's)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32], w[32];
+                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(half * 32), v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t u = static_cast<uint32_t>(c * 16 + half * 8 + i);
+                        ld_shared_cluster_v4(peer_lane + u * 512u, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        h[half * 16 + k] =
+                            pack_half2(__float_as_uint(__uint_as_float(v[2 * k]) + __uint_as_float(w[2 * k])),
+                                       __float_as_uint(__uint_as_float(v[2 * k + 1]) + __uint_as_float(w[2 * k + 1])));
+                }
+                return;
+            }
             uint32_t v0[32], v1[32];
             tmem_ld_32x32b_x32(taddr, v0);
             tmem_ld_32x32b_x32(taddr + 32, v1);
@@ -772,7 +837,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     if (lane == 0) bulk_wait_group_read<0>();
                     __syncwarp();
                     uint32_t h[32];
-                    load_chunk(tbase + static_cast<uint32_t>(c * EPI_COLS), h);
+                    load_chunk(tbase, c, h);
                     stage_chunk(buf, h);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -793,7 +858,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     for (int t = 0; t < 2; ++t) {
                         if (t < nb) {
                             uint32_t h[32];
-                            load_chunk(tbase + static_cast<uint32_t>((c + t) * EPI_COLS), h);
+                            load_chunk(tbase, c + t, h);
                             stage_chunk(bufs + t * EPI_BUF, h);
                         }
                     }
@@ -815,7 +880,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             } else {
                 for (int c = cb; c < ce; ++c) {
                     uint32_t h[32];
-                    load_chunk(tbase + static_cast<uint32_t>(c * EPI_COLS), h);
+                    load_chunk(tbase, c, h);
                     store_direct(h, row0, col_base + c * EPI_COLS);
                 }
             }
@@ -826,6 +891,37 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 if constexpr (CG == 1) mbar_arrive(bTEMPTY + 8 * i);
                 else mbar_arrive_cluster(tempty_leader + 8 * i);
             }
+            return true;
+        };
+        // K split, sender warps: wait for accumulator buffer i, stage this
+        // lane's row of it (128 fp32 columns) for the peer, arrive on the
+        // peer's recv barrier (each lane's release covers its own stores) and
+        // release the columns.  False if the wait gave up.
+        auto send = [&](uint32_t i, uint32_t par) {
+            bool got = true;
+            if (lane == 0) got = W.wait(bTFULL + 8 * i, par);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) return false;
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + i * SH::ACC_COLS;
+#pragma unroll 1
+            for (int c = 0; c < SH::ACC_COLS / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t u = static_cast<uint32_t>(c * 8 + j);
+                    const uint32_t dst = stage_lane + u * 512u;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[4 * j]),
+                                 "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                                 : "memory");
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            mbar_arrive_cluster(mapa_shared(bRECV + 8 * static_cast<uint32_t>(q & 1), krank ^ 1u));
+            if (lane == 0) mbar_arrive(bTEMPTY + 8 * i);
             return true;
         };
         uint32_t tcount = 0;
@@ -841,6 +937,17 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             if constexpr (NW == 1) {
                 const uint32_t b = tcount & 1u, aph = (tcount >> 1) & 1u;
                 const int ncols = un.half >= 0 ? SH::HALF_N : SH::ACC_COLS;
+                if (kpair) {
+                    if (sender) {
+                        if (!send(b, aph)) break;
+                        continue;
+                    }
+                    // the owner: every lane waits (its own acquire orders its
+                    // reads of the peer's rows), and the warp goes on only if
+                    // all lanes' waits completed
+                    bool got = W.template wait<true>(bRECV + 8 * static_cast<uint32_t>(q & 1), 0);
+                    if (!__all_sync(0xffffffffu, got)) break;
+                }
                 if (!drain(b, aph, b * SH::ACC_COLS, ncols, row0, col_base)) break;
             } else {
                 if (!drain(0u, used0 & 1u, 0u, SH::UMMA_N, row0, col_base)) break;
@@ -851,14 +958,19 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 }
             }
         }
-        if (lane == 0 && p.store == kStoreTma) bulk_wait_group<0>();
+        // the staging buffers must stay until the last stores have read them;
+        // the global writes themselves complete before the grid does
+        if (lane == 0 && p.store == kStoreTma) bulk_wait_group_read<0>();
         __syncwarp();
     }
 
     // ------------------------------------------------------------ tear-down
+    // (K split: the cluster barrier also keeps this CTA's staged partial sums
+    // in place until the peer has read them)
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (CG == 2) cluster_sync();
+    if (kpair && warp <= mma_warp) cluster_wait_acquire();     // the set-up barrier's wait
+    if (CG == 2 || kpair) cluster_sync();
     if (warp == mma_warp) {
         tc_fence_after_sync();
         tmem_dealloc<CG>(tmem_base, SH::TMEM_COLS);
@@ -874,20 +986,22 @@ __global__ void zero_fill_u16(unsigned short* out, int64_t n) {
         out[i] = 0;
 }
 
-// Copies the rows of lhs [ma, K] and rhs [nb, K] into rows of Kp = K rounded
-// up to 8 elements (16 bytes), the padding zeroed: a layout the tensor memory
-// accelerator can address when K * 2 bytes is not a multiple of 16 or a base
-// is not 16-byte aligned.  One thread writes one 16-byte chunk of a
-// destination row; `pairs` means 4-byte source loads are aligned (K even and
-// both bases 4-byte aligned).
+// Copies the rows of lhs [ma, K] and rhs [nb, K] into destination rows Kp
+// elements apart: a layout the tensor memory accelerator can address when
+// K * 2 bytes is not a multiple of 16 or a base is not 16-byte aligned.  The
+// first Kw = ceil(K/8)*8 elements of each row are written (the ones past K
+// zeroed); the rest of a row (Kp > Kw) is padding that keeps rows 128-byte
+// aligned and is never written or read.  One thread writes one 16-byte chunk
+// of a destination row; `pairs` means 4-byte source loads are aligned (K even
+// and both bases 4-byte aligned).
 __global__ void __launch_bounds__(256)
 repack_rows_kernel(const uint16_t* __restrict__ a, int64_t ma, const uint16_t* __restrict__ b, int64_t nb, int K,
-                   int Kp, uint16_t* __restrict__ dst_a, uint16_t* __restrict__ dst_b, int pairs) {
+                   int Kw, int Kp, uint16_t* __restrict__ dst_a, uint16_t* __restrict__ dst_b, int pairs) {
     // launched as a programmatic dependent; the GEMM that follows may start
     // its set-up while the copy finishes
     grid_dependency_wait();
     allow_dependent_launch();
-    const int64_t chunks = Kp / 8;
+    const int64_t chunks = Kw / 8;
     const int64_t total = (ma + nb) * chunks;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -930,7 +1044,14 @@ struct Plan {
     int store = kStoreTma;
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0;
     int smem = 0;
+    int ksplit = 1;             // 2: two CTAs (a cluster) per single-CTA tile, one K half each
 };
+
+// Fewest K blocks for which small single-CTA GEMMs split K over two CTAs.
+constexpr int kKSplitMinBlocks = 32;
+
+// Row alignment (elements) of the repack copy in pooled scratch.
+constexpr int64_t kPooledRowAlign = 64;
 
 // The wide tile's 48 KB slots fit the shared memory up to this many stages.
 constexpr int WIDE_MAX_STAGES = 4;
@@ -970,9 +1091,16 @@ int validate(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, 
     return GEMM_OK;
 }
 
-// Bytes of scratch the repack path needs: both operands with rows of Kp.
-inline size_t repack_bytes(int64_t M, int64_t N, int64_t K, size_t* b_offset) {
-    const int64_t Kp = (K + 7) / 8 * 8;
+// Destination row length of the repack: K rounded up to `align` elements.
+// The pooled path uses 64 (128-byte rows): on GB300 a ring-slot copy from
+// rows at a 16-byte but not 128-byte multiple runs the whole GEMM ~12 %
+// slower (4096 x 3072 x 2056: 43.6 us; with K = 2048 or 2112: 38.8 / 38.7 us).
+inline int64_t repack_ld(int64_t K, int64_t align) { return (K + align - 1) / align * align; }
+
+// Bytes of scratch the repack path needs: both operands with rows of
+// repack_ld(K, align) elements.
+inline size_t repack_bytes(int64_t M, int64_t N, int64_t K, size_t* b_offset, int64_t align) {
+    const int64_t Kp = repack_ld(K, align);
     const size_t a_bytes = (static_cast<size_t>(M) * Kp * 2 + 255) / 256 * 256;
     if (b_offset) *b_offset = a_bytes;
     return a_bytes + (static_cast<size_t>(N) * Kp * 2 + 255) / 256 * 256;
@@ -1022,6 +1150,20 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
     pl.num_kb = static_cast<int>((K + BK - 1) / BK);
     pl.smem = smem_for(stages, pl.nw);
+    // K split: where single-CTA tiles leave at least half of the SMs idle and
+    // K is long, a cluster of two CTAs computes each tile, one K half each.
+    // Small GEMMs are bound by the chain of K blocks through the ring (each
+    // block waits for a slot's load-to-use latency); halving the chain per CTA
+    // pays once it outweighs the cluster launch and the exchange of partial
+    // sums (about 2 us).  Measured on GB300 (S = 2 / 4): 1024 x 1024 x 4096
+    // 23.3 -> 17.5 / 18.2 -> 13.6 us, 512 x 512 x 8192 43.2 -> 27.4 / 32.7 ->
+    // 20.2 us, 1024 x 1024 x 2048 13.2 -> 11.4 / 10.7 -> 9.6 us; at 16 K blocks
+    // (1024^3) it is even or slower (8.0 -> 8.3 / 6.9 -> 7.6 us).  Decided
+    // from the shape alone, never from S.
+    if (pl.cg == 1 && !(flags & GEMM_DEBUG_NO_KSPLIT)) {
+        const bool forced = flags & GEMM_DEBUG_FORCE_KSPLIT;
+        if (pl.num_kb >= (forced ? 2 : kKSplitMinBlocks) && (forced || 2ll * pl.num_tiles <= num_sms)) pl.ksplit = 2;
+    }
     return pl;
 }
 
@@ -1105,15 +1247,19 @@ int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if constexpr (CG == 2) {
+    const bool kpair = CG == 1 && p.ksplit == 2;
+    if (CG == 2 || kpair) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = 2;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    const int groups = p.total_units < cap ? p.total_units : cap;
-    cfg.gridDim = dim3(CG * groups, 1, 1);
+    // K split: one cluster per tile (the staged partial sums use the ring, so
+    // a CTA never moves on to a second tile); clusters beyond what fits at
+    // once wait for the hardware to schedule them
+    const int groups = kpair ? p.total_units : (p.total_units < cap ? p.total_units : cap);
+    cfg.gridDim = dim3((kpair ? 2 : CG) * groups, 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, tc, p) != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
@@ -1161,6 +1307,7 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
     plan[7] = pl.smem;
     plan[8] = pl.num_tiles;
     plan[9] = pl.num_kb;
+    plan[10] = pl.ksplit;
     return GEMM_OK;
 }
 
@@ -1195,18 +1342,18 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     void* scratch = nullptr;
     if (pl.repack) {
         size_t b_off = 0;
-        const size_t bytes = repack_bytes(M, N, K, &b_off);
+        const size_t bytes = repack_bytes(M, N, K, &b_off, kPooledRowAlign);
         scratch = scratch_alloc(info, bytes, stream);
         if (scratch) {
-            const int64_t Kp = (K + 7) / 8 * 8;
+            const int64_t Kw = repack_ld(K, 8), Kp = repack_ld(K, kPooledRowAlign);
             uint16_t* da = static_cast<uint16_t*>(scratch);
             uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
             const int pairs = K % 2 == 0 && reinterpret_cast<uintptr_t>(lhs) % 4 == 0 &&
                               reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
-            const int64_t total = (M + N) * (Kp / 8);
+            const int64_t total = (M + N) * (Kw / 8);
             const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
             if (launch_pdl(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, lhs, M, rhs, N, static_cast<int>(K),
-                           static_cast<int>(Kp), da, db, pairs) != cudaSuccess) {
+                           static_cast<int>(Kw), static_cast<int>(Kp), da, db, pairs) != cudaSuccess) {
                 scratch_free(scratch, stream);
                 return GEMM_ERR_LAUNCH;
             }
@@ -1254,6 +1401,7 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     p.full_units = pl.num_tiles;
     p.split = 0;
     p.total_units = pl.num_tiles;
+    p.ksplit = pl.ksplit;
 
     // Tail split: when the tiles leave a last, partial wave of the persistent
     // grid (or fewer tiles than the grid) and twice that many units still
@@ -1269,7 +1417,8 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     if (cap <= 0) return done(GEMM_ERR_LAUNCH);
     const int waves = pl.num_tiles / cap;
     const int tail = pl.num_tiles - waves * cap;
-    if (pl.producer == kProducerTma && tail > 0 && 2 * tail <= cap && !(flags & GEMM_DEBUG_NO_SPLIT)) {
+    if (pl.producer == kProducerTma && pl.ksplit == 1 && tail > 0 && 2 * tail <= cap &&
+        !(flags & GEMM_DEBUG_NO_SPLIT)) {
         if (pl.nw == 1 && !encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return done(GEMM_ERR_LAUNCH);
         p.full_units = waves * cap;
         p.split = 2;
@@ -1349,7 +1498,7 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     int64_t ld = K;
     if (pl.repack) {
         size_t b_off = 0;
-        if (repack_bytes(M, N, K, &b_off) > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
+        if (repack_bytes(M, N, K, &b_off, 8) > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
         void* scratch = noalloc_scratch(info.device);
         if (!scratch) return GEMM_ERR_LAUNCH;
         // The repack writes every scratch byte the GEMM then reads (padding
@@ -1362,7 +1511,7 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
         const int64_t total = (M + N) * (Kp / 8);
         const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
         if (launch_pdl(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, lhs, M, rhs, N, static_cast<int>(K),
-                       static_cast<int>(Kp), da, db, pairs) != cudaSuccess)
+                       static_cast<int>(Kp), static_cast<int>(Kp), da, db, pairs) != cudaSuccess)
             return GEMM_ERR_LAUNCH;
         a_src = da;
         b_src = db;
@@ -1401,6 +1550,7 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     p.full_units = pl.num_tiles;        // whole tiles only
     p.split = 0;
     p.total_units = pl.num_tiles;
+    p.ksplit = pl.ksplit;               // as gemm_f16_nt: the same sums
     CUtensorMap tbh;                    // unused without the tail split
     memset(&tbh, 0, sizeof(tbh));
     return launch_plan(stages, pl, info, ta, tb, tbh, tc, p, stream);

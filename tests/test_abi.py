@@ -79,7 +79,7 @@ def test_s32_ring_argument_checks_return_before_launch(lib, args, want):
 
 
 def test_debug_flags_and_timeout_setters(lib):
-    assert lib.gemm_set_debug_flags(1 << 10) == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_debug_flags(1 << 11) == pws.GEMM_ERR_INVALID_ARG
     assert lib.gemm_set_debug_flags(0) == pws.GEMM_OK
     assert lib.gemm_set_wait_timeout_ns(0) == pws.GEMM_OK
 
@@ -119,6 +119,38 @@ def test_plan_wide_tile_rule(lib):
         # the single-CTA tile has no wide form
         pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_WIDE_TILE | pws.GEMM_DEBUG_FORCE_SOLO_TILE)
         assert (pws.gemm_f16_nt_plan(4096, 4096, 1024, stages=4)["bn"], pws.gemm_f16_nt_plan(4096, 4096, 1024, stages=4)["cta_group"]) == (128, 1)
+    finally:
+        pws.gemm_set_debug_flags(0)
+
+
+def test_plan_k_split_rule(lib):
+    # single-CTA tiles that leave at least half of the 152 SMs idle, with at
+    # least 32 K blocks: two CTAs (a cluster) per tile, one K half each.  The
+    # rule reads the shape only, never S.
+    pws.gemm_set_debug_flags(0)
+    for s in range(1, 7):
+        p = pws.gemm_f16_nt_plan(1024, 1024, 4096, stages=s)
+        assert (p["cta_group"], p["tiles"], p["k_blocks"], p["k_split"]) == (1, 64, 64, 2), s
+        assert pws.gemm_f16_nt_plan(1024, 1024, 1024, stages=s)["k_split"] == 1      # 16 K blocks
+    assert pws.gemm_f16_nt_plan(1024, 1024, 1985)["k_split"] == 2        # 32 K blocks, the last ragged
+    assert pws.gemm_f16_nt_plan(1024, 1024, 1984)["k_split"] == 1        # 31 K blocks
+    assert pws.gemm_f16_nt_plan(700, 650, 4000)["k_split"] == 2          # 6 x 6 tiles
+    assert pws.gemm_f16_nt_plan(1024, 1152, 2048)["k_split"] == 2        # 8 x 9 = 72 tiles: 144 CTAs
+    assert pws.gemm_f16_nt_plan(1024, 1216, 2048)["k_split"] == 1        # 8 x 10 = 80 tiles: 160 CTAs > 152
+    assert pws.gemm_f16_nt_plan(4096, 4096, 4096)["k_split"] == 1        # pair tiles
+    assert pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)["k_split"] == 1
+    assert pws.gemm_f16_nt_plan(65, 70, 2051)["k_split"] == 2            # repacked operands
+    try:
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
+        assert pws.gemm_f16_nt_plan(700, 650, 4000)["k_split"] == 2
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_NO_KSPLIT)
+        assert pws.gemm_f16_nt_plan(1024, 1024, 4096)["k_split"] == 1
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE)
+        assert pws.gemm_f16_nt_plan(1024, 1024, 4096)["k_split"] == 1
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_KSPLIT | pws.GEMM_DEBUG_FORCE_SOLO_TILE)
+        assert pws.gemm_f16_nt_plan(4096, 4096, 1024)["k_split"] == 2        # 1024 tiles
+        assert pws.gemm_f16_nt_plan(300, 300, 128)["k_split"] == 2           # 2 K blocks
+        assert pws.gemm_f16_nt_plan(300, 300, 64)["k_split"] == 1            # 1 K block
     finally:
         pws.gemm_set_debug_flags(0)
 

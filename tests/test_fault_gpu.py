@@ -31,13 +31,18 @@ def gpu():
 @pytest.mark.parametrize("extra,N", [
     (0, 256), (pws.GEMM_DEBUG_FORCE_PAIR_TILE, 256), (pws.GEMM_DEBUG_FORCE_COPY_PRODUCER, 256),
     (pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE, 512),   # split accumulator, 8 epilogue warps
-], ids=["solo_tma", "pair_tma", "solo_copy", "wide_tma"])
+    (pws.GEMM_DEBUG_FORCE_KSPLIT, 256),                 # two CTAs per tile, one K half each
+    (pws.GEMM_DEBUG_FORCE_KSPLIT | pws.GEMM_DEBUG_FORCE_COPY_PRODUCER, 256),
+], ids=["solo_tma", "pair_tma", "solo_copy", "wide_tma", "ksplit_tma", "ksplit_copy"])
 def test_missing_seed_times_out_and_context_survives(seed_flag, extra, N):
     # Without the empty seed the producer's first wait never completes: no
     # copy is ever issued.  Without the accumulator seed the multiply role's
     # first wait never completes while the producer has filled both slots
     # (K = 256 is four K blocks, S = 2): the roles give up with copies
-    # issued, and a pair's producers drain them before the CTAs exit.
+    # issued, and a pair's producers drain them before the CTAs exit.  With the
+    # K split, the owner warps' wait for the peer's partial sums gives up too
+    # (their own CTA's abort, or the time limit), and every CTA meets its peer
+    # at the cluster barrier before exiting.
     M, K = 256, 256
     a_np = inputs.uniform_f16(2, 0, (M, K))
     b_np = inputs.uniform_f16(2, 1, (N, K))
