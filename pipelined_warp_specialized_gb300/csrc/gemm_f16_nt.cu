@@ -50,6 +50,11 @@
 // computes 128 x 128.  The tile is chosen from the shape and S alone, and
 // every tile sums each output element over K in the same order.
 //
+// Small outputs with a long K split it instead: a cluster of two single CTAs
+// per 128 x 128 tile, each summing one K half into its own accumulator; the
+// two fp32 partial sums meet over distributed shared memory and are added
+// once before the rounding.  That choice reads M, N and K only.
+//
 // Grids are launched as programmatic dependents: set-up (barriers, tensor
 // memory, cluster) overlaps the previous grid on the stream, and global
 // memory is touched only once that grid has completed.
