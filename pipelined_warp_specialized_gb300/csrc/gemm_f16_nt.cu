@@ -738,27 +738,32 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         // K split.  Lane quarters 2*krank and 2*krank+1 of the tile are this
         // CTA's to store.  The warps of the other two quarters are senders:
-        // they copy their fp32 partial sums into this CTA's ring (idle once
-        // the accumulator is complete; one tile per CTA) and arrive on the
-        // peer's recv barrier, whose owner warp adds them to its own partial
-        // sums before rounding.  Staged layout, 16 KB per quarter: 16-byte
-        // unit u (fp32 columns 4u..4u+3) of lane l's row at u * 512 + l * 16,
-        // so that one unit of all 32 rows is one contiguous 512-byte block:
-        // conflict-free to write, and a single request for the peer to read
-        // (read from a 512-byte row per lane, the peer's loads measured 3-4x
-        // slower on GB300).
+        // they write their fp32 partial sums from registers straight into the
+        // peer's epilogue staging area and arrive on the peer's recv barrier
+        // (each lane's release publishes its own stores); the owner warp then
+        // adds them, read locally, to its own partial sums before rounding.
+        // The staging area is free for this from the start: the K split's
+        // owners stage their f16 output in their own ring instead (idle once
+        // their accumulator is complete; one tile per CTA).  Layout, 16 KB per
+        // quarter: 16-byte unit u (fp32 columns 4u..4u+3) of lane l's row at
+        // u * 512 + l * 16, so one unit of all 32 rows is one contiguous
+        // 512-byte block (conflict-free, one request per warp).  Measured on
+        // GB300: the owner reading the sums from the peer instead cost about
+        // 2 us more per tile, each remote round trip exposed.
         const bool sender = kpair && static_cast<uint32_t>(q >> 1) != krank;
-        const uint32_t stage_lane = sA + static_cast<uint32_t>(q & 1) * (32u * 512u) + static_cast<uint32_t>(lane) * 16u;
-        const uint32_t peer_lane = kpair && !sender ? mapa_shared(stage_lane, krank ^ 1u) : 0u;
-        static_assert(SH::ACC_COLS / 4 * 512 <= 32 * 512 || CG == 2, "a staged quarter holds the single tile's 128 fp32 columns");
-        static_assert(2 * 32 * 512 <= A_SLOT + B_SLOT, "two staged quarters fit in the smallest ring");
+        const uint32_t recv_lane = sEPI + static_cast<uint32_t>(q & 1) * (32u * 512u) + static_cast<uint32_t>(lane) * 16u;
+        const uint32_t push_lane = sender ? mapa_shared(recv_lane, krank ^ 1u) : 0u;
+        const uint32_t peer_sums = kpair && !sender ? recv_lane : 0u;
+        static_assert(SH::ACC_COLS / 4 * 512 <= 32 * 512 || CG == 2, "a received quarter holds the single tile's 128 fp32 columns");
+        static_assert(2 * 32 * 512 == EPI_BYTES, "the staging area holds the two received quarters");
+        static_assert(EPI_WARPS * 2 * EPI_BUF <= A_SLOT + B_SLOT, "the owners' output staging fits in the smallest ring");
         // Reads 64 accumulator columns (chunk c of the columns starting at
         // tensor-memory address tbase) of this lane's row, adds the peer's
         // partial sums of the same columns (K split), and rounds them to 32
         // packed f16 pairs.
         auto load_chunk = [&](uint32_t tbase, int c, uint32_t(&h)[32]) {
             const uint32_t taddr = tbase + static_cast<uint32_t>(c * EPI_COLS);
-            if (peer_lane) {
+            if (peer_sums) {
                 // 32 columns at a time: own partial sums from tensor memory and
                 // the peer's (units 16c + 8 half ..+7) in flight together, then
                 // own + peer, one fp32 add per element (commutative, so the
@@ -770,7 +775,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint32_t u = static_cast<uint32_t>(c * 16 + half * 8 + i);
-                        ld_shared_cluster_v4(peer_lane + u * 512u, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        ld_shared_v4(peer_sums + u * 512u, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     }
                     tmem_ld_wait();
 #pragma unroll
@@ -853,7 +858,9 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     }
                 }
             } else if (p.store == kStoreTma) {
-                const uint32_t bufs = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF;
+                // (the K split's owners stage in their ring: the staging area
+                // holds the peer's partial sums)
+                const uint32_t bufs = (kpair ? sA : sEPI) + static_cast<uint32_t>(e) * 2 * EPI_BUF;
                 for (int c = 0; c < nch; c += 2) {
                     const int nb = nch - c < 2 ? nch - c : 2;
                     // the stores issued from both buffers have finished reading them
@@ -898,10 +905,10 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             }
             return true;
         };
-        // K split, sender warps: wait for accumulator buffer i, stage this
-        // lane's row of it (128 fp32 columns) for the peer, arrive on the
-        // peer's recv barrier (each lane's release covers its own stores) and
-        // release the columns.  False if the wait gave up.
+        // K split, sender warps: wait for accumulator buffer i, write this
+        // lane's row of it (128 fp32 columns) into the peer's staging area,
+        // arrive on the peer's recv barrier and release the columns.  False
+        // if the wait gave up.
         auto send = [&](uint32_t i, uint32_t par) {
             bool got = true;
             if (lane == 0) got = W.wait(bTFULL + 8 * i, par);
@@ -910,18 +917,19 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + i * SH::ACC_COLS;
 #pragma unroll 1
-            for (int c = 0; c < SH::ACC_COLS / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), v);
+            for (int c = 0; c < SH::ACC_COLS / 64; ++c) {
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 64), v0);
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 64 + 32), v1);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t u = static_cast<uint32_t>(c * 8 + j);
-                    const uint32_t dst = stage_lane + u * 512u;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[4 * j]),
-                                 "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
-                                 : "memory");
-                }
+                for (int j = 0; j < 8; ++j)
+                    st_shared_cluster_v4(push_lane + static_cast<uint32_t>(c * 16 + j) * 512u, v0[4 * j],
+                                         v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_cluster_v4(push_lane + static_cast<uint32_t>(c * 16 + 8 + j) * 512u, v1[4 * j],
+                                         v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -1160,10 +1168,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     // Small GEMMs are bound by the chain of K blocks through the ring (each
     // block waits for a slot's load-to-use latency); halving the chain per CTA
     // pays once it outweighs the cluster launch and the exchange of partial
-    // sums (about 2 us).  Measured on GB300 (S = 2 / 4): 1024 x 1024 x 4096
-    // 23.3 -> 17.5 / 18.2 -> 13.6 us, 512 x 512 x 8192 43.2 -> 27.4 / 32.7 ->
-    // 20.2 us, 1024 x 1024 x 2048 13.2 -> 11.4 / 10.7 -> 9.6 us; at 16 K blocks
-    // (1024^3) it is even or slower (8.0 -> 8.3 / 6.9 -> 7.6 us).  Decided
+    // sums (about 1.5 us).  Measured on GB300 (S = 2 / 4): 1024 x 1024 x 4096
+    // 23.4 -> 17.0 / 18.1 -> 13.2 us, 512 x 512 x 8192 43.1 -> 26.5 / 32.6 ->
+    // 19.7 us, 1024 x 1024 x 2048 13.2 -> 10.9 / 10.7 -> 9.3 us; at 16 K blocks
+    // (1024^3) it is even or slower (8.0 -> 7.9 / 6.9 -> 7.3 us).  Decided
     // from the shape alone, never from S.
     if (pl.cg == 1 && !(flags & GEMM_DEBUG_NO_KSPLIT)) {
         const bool forced = flags & GEMM_DEBUG_FORCE_KSPLIT;

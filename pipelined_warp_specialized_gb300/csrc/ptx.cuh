@@ -101,16 +101,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-// 16 bytes from the shared memory of a CTA of the cluster (an address from
-// mapa_shared); the caller orders it after the writer's release.
-__device__ __forceinline__ void ld_shared_cluster_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c,
-                                                     uint32_t& d) {
-    asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-                 : "r"(addr)
-                 : "memory");
-}
-
 // The two halves of a cluster barrier, for a thread with work to do between
 // them: every thread of the cluster arrives once, and waits before it arrives
 // again.
@@ -120,6 +110,21 @@ __device__ __forceinline__ void cluster_arrive_release() {
 
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 16 bytes into the shared memory of a CTA of the cluster (an address from
+// mapa_shared); a later release (e.g. mbarrier.arrive.release.cluster)
+// publishes it.
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(addr)
+                 : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {

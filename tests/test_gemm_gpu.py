@@ -213,11 +213,12 @@ KS = pws.GEMM_DEBUG_FORCE_KSPLIT
     (2048, 2048, 512, KS | pws.GEMM_DEBUG_FORCE_SOLO_TILE),   # 256 clusters: more than fit at once
 ])
 def test_f16_k_split(M, N, K, flags):
-    # A cluster of two CTAs per single-CTA tile, one K half each; the owner of
-    # each lane quarter adds the peer's fp32 partial sums over distributed
-    # shared memory before rounding.  Checked against the oracle for S = 1, 2
-    # and 6 (the smallest ring, whose 32 KB hold the two staged quarters
-    # exactly, and the paired-slot MMA loop), bitwise equal across them.
+    # A cluster of two CTAs per single-CTA tile, one K half each; the senders
+    # of each lane quarter write their fp32 partial sums into the owner's
+    # shared memory, where the owner adds them before rounding.  Checked
+    # against the oracle for S = 1, 2 and 6 (the smallest ring, whose 32 KB
+    # hold the owners' output staging exactly, and the paired-slot MMA loop),
+    # bitwise equal across them.
     pws.gemm_set_debug_flags(flags)
     try:
         assert pws.gemm_f16_nt_plan(M, N, K, stages=2)["k_split"] == 2
