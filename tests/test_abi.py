@@ -24,6 +24,22 @@ def test_exports_every_declared_function(lib):
         assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
 
 
+def test_binding_constants_match_the_header():
+    # every GEMM_* enumerator the header declares has the same value in the
+    # binding, and the binding defines no GEMM_* constant the header lacks
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(pws.__file__), os.pardir, "include", "pwsgemm.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    declared = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"\b(GEMM_[A-Z_]+)\s*=\s*(\d+)u?\b", hdr)}
+    assert "GEMM_DEBUG_FORCE_KSPLIT" in declared and "GEMM_ERR_TIMEOUT" in declared
+    bound = {k: v for k, v in vars(pws).items() if k.startswith("GEMM_") and isinstance(v, int)}
+    assert bound == declared
+    # the debug flags are distinct single bits
+    flags = [v for k, v in declared.items() if k.startswith("GEMM_DEBUG_")]
+    assert all(f and f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)
+
+
 def test_status_strings(lib):
     for code, name in [(0, "GEMM_OK"), (1, "GEMM_ERR_INVALID_ARG"), (2, "GEMM_ERR_ALIGNMENT"),
                        (3, "GEMM_ERR_UNSUPPORTED_STAGES"), (4, "GEMM_ERR_UNSUPPORTED_ARCH"),
