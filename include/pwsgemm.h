@@ -137,13 +137,19 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  * store.
  *
  * Output tiles: 256 x 256 on a CTA pair (two SMs sharing one tcgen05 MMA),
- * or 128 x 128 on one CTA for outputs too small to occupy the GPU with pairs
- * and for the asynchronous-copy producer.  With stages <= 4 the pair uses a
- * 256 x 512 tile instead where that adds no padding columns: each ring slot
- * then carries two B boxes, so each operand byte copied into shared memory
- * feeds 4/3 as many flops (5 and 6 slots of that size do not fit in shared
- * memory).  Every tile sums each output element over K in the same order,
- * so the tile choice never changes the result.
+ * or 128 x 128 on one CTA.  The pair tile is used when TMA feeds it and it
+ * needs fewer waves of CTA groups than the single-CTA tile (or as many, with
+ * at least as many pair tiles as half the SMs); the asynchronous-copy
+ * producer always uses the single-CTA tile.  With stages <= 4 the pair uses
+ * a 256 x 512 tile instead where that adds no padding columns: each ring
+ * slot then carries two B boxes, so each operand byte copied into shared
+ * memory feeds 4/3 as many flops (5 and 6 slots of that size do not fit in
+ * shared memory).  The 256 x 256 tile is kept where the 256 x 512 one would
+ * leave pairs idle that it fills: when its tiles fit in one wave of pairs,
+ * or, with 3 or 4 slots, when the 256 x 512 tiles are fewer than the pairs
+ * and the 256 x 256 ones take one wave and a tail of at most half of it.
+ * Every tile sums each output element over K in the same order, so the tile
+ * choice never changes the result.
  *
  * K split: when the 128 x 128 tile is used, the tiles fill at most half of
  * the SMs and K spans at least 32 blocks of 64 (K > 1984), each tile is

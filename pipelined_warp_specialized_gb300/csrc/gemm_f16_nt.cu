@@ -1126,6 +1126,22 @@ inline size_t repack_bytes(int64_t M, int64_t N, int64_t K, size_t* b_offset, in
 // would add a block of padding columns the 256-column tiles do not have.
 bool want_wide(int64_t N) { return (N + 511) / 512 * 2 == (N + 255) / 256; }
 
+// Where the wide tile would leave CTA pairs idle that the 256 x 256 tile
+// fills (both give the same bits, so S may decide): when the 256 x 256 tiles
+// fit in one wave of pairs (the wide ones would need the half split to fill
+// them), or, from three slots on, when the wide tiles are fewer than the
+// pairs while the 256 x 256 tiles take one wave and a tail that the half
+// split runs at once.  Measured on GB300: 2048^2 x 4096, S = 1..4: 256 x 256
+// 2-8 % faster; 2560^3, S = 3 / 4: 27.6 / 25.7 us against 29.9 / 29.9 us
+// (at S = 1, 2 the wide tile wins: 56.5 / 32.5 against 65.2 / 36.5 us).
+// Elsewhere the wide tile was as fast or faster (3072^3 to 8192^3).
+bool narrow_fills_better(int64_t M, int64_t N, int stages, int64_t pair_cap) {
+    const int64_t narrow = ((M + 255) / 256) * ((N + 255) / 256);
+    const int64_t wide = ((M + 255) / 256) * ((N + 511) / 512);
+    if (narrow <= pair_cap) return true;
+    return stages >= 3 && wide < pair_cap && 2 * (narrow - pair_cap) <= pair_cap;
+}
+
 // `allow_repack` = false plans the path that needs no scratch memory.
 Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, const void* out, int stages,
                int num_sms, unsigned flags, bool allow_repack = true) {
@@ -1148,13 +1164,26 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
         else pl.copy_bytes = 2;
     }
     pl.store = (!(flags & GEMM_DEBUG_FORCE_DIRECT_STORE) && N % 8 == 0 && o % 16 == 0) ? kStoreTma : kStoreDirect;
-    // The CTA-pair tile when TMA feeds it and there are enough pair tiles to
-    // occupy the GPU; otherwise the single-CTA tile.
+    // The CTA-pair tile when TMA feeds it and it needs fewer waves of the
+    // persistent grid than the single-CTA tile (or as many, with enough pair
+    // tiles to occupy the GPU); otherwise the single-CTA tile.  Small and
+    // mid-size GEMMs are bound by each CTA's chain of K blocks through the
+    // ring more than by the multiplies, so the wave count decides: a pair
+    // block does twice a single CTA's work in about 1.2x the time.  Measured
+    // on GB300 (S = 2 / 4): 2048^3 on 64 pair tiles (one wave) 18.6 / 13.9
+    // us, on 256 single tiles (two waves) 27.5 / 19.3 us.  Decided from the
+    // shape alone; the single-CTA tile keeps every shape the K split uses.
+    const int64_t solo_tiles = ((M + 127) / 128) * ((N + 127) / 128);
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    const bool want_pair = (flags & GEMM_DEBUG_FORCE_PAIR_TILE) || 2 * pair_tiles >= num_sms;
+    const int64_t pair_cap = num_sms / 2;
+    const int64_t solo_waves = (solo_tiles + num_sms - 1) / num_sms;
+    const int64_t pair_waves = (pair_tiles + pair_cap - 1) / pair_cap;
+    const bool want_pair = (flags & GEMM_DEBUG_FORCE_PAIR_TILE) || pair_waves < solo_waves ||
+                           (pair_waves == solo_waves && 2 * pair_tiles >= num_sms);
     pl.cg = (pl.producer == kProducerTma && !(flags & GEMM_DEBUG_FORCE_SOLO_TILE) && want_pair) ? 2 : 1;
     pl.nw = (pl.cg == 2 && stages <= WIDE_MAX_STAGES && !(flags & GEMM_DEBUG_FORCE_NARROW_TILE) &&
-             ((flags & GEMM_DEBUG_FORCE_WIDE_TILE) || want_wide(N)))
+             ((flags & GEMM_DEBUG_FORCE_WIDE_TILE) ||
+              (want_wide(N) && !narrow_fills_better(M, N, stages, pair_cap))))
                 ? 2
                 : 1;
     const int tile_m = 128 * pl.cg, tile_n = 128 * pl.cg * pl.nw;

@@ -139,6 +139,29 @@ def test_plan_wide_tile_rule(lib):
         pws.gemm_set_debug_flags(0)
 
 
+def test_plan_wave_count_rules(lib):
+    # pair tiles where they need fewer waves of the grid than single tiles
+    # (152 SMs: 76 pairs), whatever S; ties keep the old rule
+    pws.gemm_set_debug_flags(0)
+    def tile(M, N, K, s):
+        p = pws.gemm_f16_nt_plan(M, N, K, stages=s)
+        return p["bm"], p["bn"]
+    for s in range(1, 7):
+        assert tile(2048, 2048, 2048, s) == (256, 256)      # 64 pair tiles (1 wave) vs 256 single (2)
+        assert tile(1024, 4096, 2048, s) == (256, 256)
+        assert tile(1536, 1536, 1536, s) == (128, 128)      # 1 wave either way, 36 pair tiles
+        assert tile(1024, 1024, 1024, s) == (128, 128)
+    # the wide tile gives way to 256 x 256 where that fills the pairs better
+    # (same bits either way, so S may decide)
+    for s in range(1, 5):
+        assert tile(2048, 2048, 4096, s) == (256, 256)      # 64 narrow tiles fit one wave
+        assert tile(2560, 2560, 2560, s) == ((256, 512) if s <= 2 else (256, 256))
+        assert tile(3072, 3072, 3072, s) == (256, 512)      # narrow tail of 68 does not half-split
+        assert tile(4096, 4096, 4096, s) == (256, 512)
+        assert tile(2048, 4096, 4096, s) == (256, 512)
+        assert tile(8192, 8192, 8192, s) == (256, 512)
+
+
 def test_plan_k_split_rule(lib):
     # single-CTA tiles that leave at least half of the 152 SMs idle, with at
     # least 32 K blocks: two CTAs (a cluster) per tile, one K half each.  The
