@@ -999,53 +999,87 @@ __global__ void zero_fill_u16(unsigned short* out, int64_t n) {
         out[i] = 0;
 }
 
+// Bytes sh .. sh+15 (sh even) of the 32 bytes lo | hi, little-endian.
+__device__ __forceinline__ uint4 bytes_at(const uint4& lo, const uint4& hi, unsigned sh) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const unsigned q = sh >> 2, bits = (sh & 3u) * 8u;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t x = q == 0 ? w[i] : q == 1 ? w[i + 1] : q == 2 ? w[i + 2] : w[i + 3];
+        const uint32_t y = q == 0 ? w[i + 1] : q == 1 ? w[i + 2] : q == 2 ? w[i + 3] : w[i + 4];
+        o[i] = __funnelshift_r(x, y, bits);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Copies the rows of lhs [ma, K] and rhs [nb, K] into destination rows Kp
 // elements apart: a layout the tensor memory accelerator can address when
 // K * 2 bytes is not a multiple of 16 or a base is not 16-byte aligned.  The
 // first Kw = ceil(K/8)*8 elements of each row are written (the ones past K
 // zeroed); the rest of a row (Kp > Kw) is padding that keeps rows 128-byte
-// aligned and is never written or read.  One thread writes one 16-byte chunk
-// of a destination row; `pairs` means 4-byte source loads are aligned (K even
-// and both bases 4-byte aligned).
+// aligned and is never written or read.
+//
+// A row is copied by 2^tpr_log2 threads (as many as it has 16-byte chunks,
+// up to the 256 of a block; a block takes 256 >> tpr_log2 rows), thread t
+// writing chunks t, t + 2^tpr_log2, ...  A chunk wholly inside the row is
+// read as the aligned 16-byte blocks that hold it (one, or two when the row
+// does not start on a 16-byte boundary) and shifted into place; every block
+// read holds at least one byte of the row, so no load leaves the pages the
+// operand occupies.  The ragged last chunk of a row is read element by
+// element.  The copy is bound by memory bandwidth (57.6 MB moved for the
+// 4000 x 3000 x 2050 operands, about 6 TB/s): a thread per chunk with 4-byte
+// loads and a 64-bit division per chunk ran as fast, one warp per row (9
+// dependent rounds of loads) about 1 us slower.
 __global__ void __launch_bounds__(256)
 repack_rows_kernel(const uint16_t* __restrict__ a, int64_t ma, const uint16_t* __restrict__ b, int64_t nb, int K,
-                   int Kw, int Kp, uint16_t* __restrict__ dst_a, uint16_t* __restrict__ dst_b, int pairs) {
+                   int Kw, int Kp, uint16_t* __restrict__ dst_a, uint16_t* __restrict__ dst_b, int tpr_log2) {
     // launched as a programmatic dependent; the GEMM that follows may start
     // its set-up while the copy finishes
     grid_dependency_wait();
     allow_dependent_launch();
-    const int64_t chunks = Kw / 8;
-    const int64_t total = (ma + nb) * chunks;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        int64_t r = i / chunks;
-        const int k0 = static_cast<int>(i - r * chunks) * 8;
-        const uint16_t* src;
-        uint16_t* dst;
-        if (r < ma) {
-            src = a + r * K;
-            dst = dst_a + r * Kp;
+    const int tpr = 1 << tpr_log2;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> tpr_log2) + (threadIdx.x >> tpr_log2);
+    if (r >= ma + nb) return;
+    const int t = threadIdx.x & (tpr - 1);
+    const int chunks = Kw / 8, full = K / 8;
+    const uint16_t* src = r < ma ? a + r * K : b + (r - ma) * K;
+    uint16_t* dst = r < ma ? dst_a + r * Kp : dst_b + (r - ma) * Kp;
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+    const unsigned sh = static_cast<unsigned>(sa & 15u);      // even: the operands are 2-byte aligned
+    const uint4* blk = reinterpret_cast<const uint4*>(sa - sh);
+    for (int j = t; j < chunks; j += tpr) {
+        uint4 o;
+        if (j < full) {
+            const uint4 lo = blk[j];
+            o = sh == 0 ? lo : bytes_at(lo, blk[j + 1], sh);
         } else {
-            r -= ma;
-            src = b + r * K;
-            dst = dst_b + r * Kp;
-        }
-        uint32_t w[4];
-        if (pairs && k0 + 8 <= K) {
-            const uint32_t* s4 = reinterpret_cast<const uint32_t*>(src + k0);
+            uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = __ldg(s4 + j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int k = k0 + 2 * j;
-                const uint32_t lo = k < K ? __ldg(src + k) : 0u;
-                const uint32_t hi = k + 1 < K ? __ldg(src + k + 1) : 0u;
-                w[j] = lo | (hi << 16);
+            for (int e = 0; e < 4; ++e) {
+                const int k = 8 * j + 2 * e;
+                const uint32_t lo16 = k < K ? src[k] : 0u;
+                const uint32_t hi16 = k + 1 < K ? src[k + 1] : 0u;
+                w[e] = lo16 | (hi16 << 16);
             }
+            o = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(dst + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + 8 * static_cast<int64_t>(j)) = o;
     }
+}
+
+// Launches repack_rows_kernel over the M + N rows (Kw elements written per
+// destination row, rows Kp elements apart).
+cudaError_t launch_repack(const void* lhs, int64_t M, const void* rhs, int64_t N, int64_t K, int64_t Kw, int64_t Kp,
+                          uint16_t* da, uint16_t* db, cudaStream_t stream) {
+    int tpr_log2 = 0;
+    while ((1 << tpr_log2) < Kw / 8 && tpr_log2 < 8) ++tpr_log2;
+    const int64_t rows_per_block = 256 >> tpr_log2;
+    const int64_t blocks = (M + N + rows_per_block - 1) / rows_per_block;
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+    return launch_pdl(repack_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                      static_cast<const uint16_t*>(lhs), M, static_cast<const uint16_t*>(rhs), N, static_cast<int>(K),
+                      static_cast<int>(Kw), static_cast<int>(Kp), da, db, tpr_log2);
 }
 
 struct Plan {
@@ -1390,12 +1424,7 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
             const int64_t Kw = repack_ld(K, 8), Kp = repack_ld(K, kPooledRowAlign);
             uint16_t* da = static_cast<uint16_t*>(scratch);
             uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
-            const int pairs = K % 2 == 0 && reinterpret_cast<uintptr_t>(lhs) % 4 == 0 &&
-                              reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
-            const int64_t total = (M + N) * (Kw / 8);
-            const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
-            if (launch_pdl(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, lhs, M, rhs, N, static_cast<int>(K),
-                           static_cast<int>(Kw), static_cast<int>(Kp), da, db, pairs) != cudaSuccess) {
+            if (launch_repack(lhs, M, rhs, N, K, Kw, Kp, da, db, stream) != cudaSuccess) {
                 scratch_free(scratch, stream);
                 return GEMM_ERR_LAUNCH;
             }
@@ -1548,12 +1577,7 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
         const int64_t Kp = (K + 7) / 8 * 8;
         uint16_t* da = static_cast<uint16_t*>(scratch);
         uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
-        const int pairs = K % 2 == 0 && reinterpret_cast<uintptr_t>(lhs) % 4 == 0 &&
-                          reinterpret_cast<uintptr_t>(rhs) % 4 == 0;
-        const int64_t total = (M + N) * (Kp / 8);
-        const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 16ll * info.num_sms));
-        if (launch_pdl(repack_rows_kernel, dim3(blocks), dim3(256), 0, stream, lhs, M, rhs, N, static_cast<int>(K),
-                       static_cast<int>(Kp), static_cast<int>(Kp), da, db, pairs) != cudaSuccess)
+        if (launch_repack(lhs, M, rhs, N, K, Kp, Kp, da, db, stream) != cudaSuccess)
             return GEMM_ERR_LAUNCH;
         a_src = da;
         b_src = db;
