@@ -34,6 +34,7 @@ from __future__ import annotations
 
 import argparse
 import datetime
+import functools
 import hashlib
 import json
 import os
@@ -333,7 +334,7 @@ def concurrency_configs(pws, torch, G=16, stream_counts=(1, 2, 4, 8)):
     out = {}
     dev = torch.device("cuda")
     wl = inputs.WORKLOADS["f16_nt_1024"]
-    a, b = torch.from_numpy(wl.lhs()).to(dev), torch.from_numpy(wl.rhs()).to(dev)
+    a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(wl.name))
     outs = [torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev) for _ in range(G)]
     wl2 = inputs.WORKLOADS["s32_nn_128x256x256"]
     a2, b2 = torch.from_numpy(wl2.lhs()).to(dev), torch.from_numpy(wl2.rhs()).to(dev)
@@ -364,8 +365,7 @@ def extra_configs(pws, torch, stream):
     out = {}
     dev = torch.device("cuda")
     wl = inputs.WORKLOADS["s32_nn_128x256x256"]
-    a = torch.from_numpy(wl.lhs()).to(dev)
-    b = torch.from_numpy(wl.rhs()).to(dev)
+    a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(wl.name))
     c = torch.empty(wl.M, wl.N, dtype=torch.int32, device=dev)
     ms_eager = time_launches(lambda: pws.gemm_s32_nn(a, b, c, stream=stream), 200, 20, torch, stream)
     ms = time_graph(lambda st: pws.gemm_s32_nn(a, b, c, stream=st), torch)
@@ -379,8 +379,7 @@ def extra_configs(pws, torch, stream):
     out[wl.name + "/ring"] = ring
     for name in ("f16_nt_1024", "f16_nt_4096", "f16_nt_ragged_4000x3000x2050", "f16_nt_8192"):
         wl = inputs.WORKLOADS[name]
-        a = torch.from_numpy(wl.lhs()).to(dev)
-        b = torch.from_numpy(wl.rhs()).to(dev)
+        a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(name))
         c = torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev)
         # the ragged shape is timed on both of its paths: repack + TMA (the
         # default) and the async-copy producer reading the operands in place
@@ -529,6 +528,14 @@ def run_ours(args, world, rank, local):
 
 # ---------------------------------------------------------------- CPU oracle
 
+@functools.lru_cache(maxsize=None)
+def workload_inputs(name):
+    """The seeded operands of one of the smaller workloads, generated once per
+    process (the configs' timings and the oracle's share them)."""
+    wl = inputs.WORKLOADS[name]
+    return wl.lhs(), wl.rhs()
+
+
 def oracle_time(a, b, rows):
     """Times the oracle on the first `rows` rows of lhs against all of rhs."""
     import oracle
@@ -548,7 +555,28 @@ def cpu_baseline(M, N, K, seconds, a, b):
     t = oracle_time(a, b, rows)
     flops = 2.0 * rows * N * K
     return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows} of {M} output rows x {N} columns, K={K} (f64 triple loop), {t:.1f} s"}
+            "sample": f"{rows} of {M} output rows x {N} columns, K={K} (f64 triple loop), {t:.1f} s",
+            "per_config": oracle_per_config(threads)}
+
+
+def oracle_per_config(threads):
+    """The oracle on each smaller workload, whole (seconds and GFLOP/s, all
+    host threads), and on the 1024^3 one with a single thread: about 6 s."""
+    import oracle
+    out = {}
+    runs = [(name, threads) for name in ("s32_nn_128x256x256", "f16_nt_1024", "f16_nt_ragged_4000x3000x2050",
+                                         "f16_nt_4096")]
+    runs.append(("f16_nt_1024", 1))
+    for name, nt in runs:
+        wl = inputs.WORKLOADS[name]
+        a, b = workload_inputs(name)
+        fn = oracle.gemm_s32_nn if name.startswith("s32") else oracle.gemm_f16_nt_f64
+        t0 = time.perf_counter()
+        fn(a, b, nthreads=nt)
+        dt = time.perf_counter() - t0
+        key = name if nt == threads else f"{name}/1_thread"
+        out[key] = {"s": round(dt, 4), "GFLOP_s": round(wl.flops / dt / 1e9, 2), "threads": nt}
+    return out
 
 
 def run_reference(args, world, rank):
