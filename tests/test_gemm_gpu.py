@@ -349,6 +349,26 @@ def test_f16_unaligned_operands(flags):
     assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b), K)
 
 
+@pytest.mark.parametrize("offset", range(8))
+def test_f16_repack_every_row_alignment(offset):
+    # The repack reads each row as the aligned 16-byte blocks that hold it and
+    # shifts them into place.  lhs starts `offset` elements into a buffer and
+    # rhs 7 - offset; with K odd, consecutive rows start 2 bytes further on,
+    # so every even byte offset 0..14 occurs as a row start, for both
+    # operands, and the last rows end near the buffers' ends.
+    M, N, K = 37, 45, 1027
+    big_a = _dev(inputs.normal_f16(60 + offset, 0, (M * K + 8,)))
+    big_b = _dev(inputs.normal_f16(60 + offset, 1, (N * K + 8,)))
+    a_t = big_a[offset:offset + M * K].view(M, K)
+    b_t = big_b[7 - offset:7 - offset + N * K].view(N, K)
+    assert pws.gemm_f16_nt_plan(M, N, K, a_t.data_ptr(), b_t.data_ptr(), 3 << 40)["producer"] == 2
+    for fn in (pws.gemm_f16_nt, pws.gemm_f16_nt_noalloc):
+        out = fn(a_t, b_t, stages=2)
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_OK
+        assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b_t.cpu().numpy()), K)
+
+
 @pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER])
 def test_f16_closed_forms_bit_exact(flags):
     # rank one with dyadic values: every sum is K * a_m * b_n, exact in fp32 and in f16
