@@ -162,6 +162,14 @@ def test_plan_wave_count_rules(lib):
         assert tile(8192, 8192, 8192, s) == (256, 512)
 
 
+def test_smoke_cases_plan_the_paths_they_check(lib):
+    # smoke() runs on the GPU only at round end; its plan expectations are
+    # host logic and are checked here first
+    import __graft_entry__
+    pws.gemm_set_debug_flags(0)
+    __graft_entry__.check_smoke_plans()
+
+
 def test_plan_k_split_rule(lib):
     # single-CTA tiles that leave at least half of the 152 SMs idle, with at
     # least 32 K blocks: two CTAs (a cluster) per tile, one K half each.  The
