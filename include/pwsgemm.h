@@ -171,7 +171,9 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  *
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT (a pointer not
  * 2-byte aligned), GEMM_ERR_UNSUPPORTED_STAGES, GEMM_ERR_UNSUPPORTED_ARCH or
- * GEMM_ERR_LAUNCH.  M, N, K must each be below 2^31.
+ * GEMM_ERR_LAUNCH.  M, N, K must each be below 2^31, and the output must
+ * hold fewer than 2^31 tiles of 128 x 128 (ceil(M/128) * ceil(N/128)), else
+ * GEMM_ERR_INVALID_ARG.
  */
 int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                 gemm_f16_t* out, int stages, cudaStream_t stream);

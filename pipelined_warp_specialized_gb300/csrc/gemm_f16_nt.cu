@@ -1128,6 +1128,9 @@ int validate(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, 
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
     if (stages < 1 || stages > MAX_STAGES) return GEMM_ERR_UNSUPPORTED_STAGES;
     if (M == 0 || N == 0) return GEMM_OK;
+    // the plan counts 128 x 128 tiles in an int (no output that large fits in
+    // any device's memory: it would hold 2^31 * 2^14 elements)
+    if (((M + 127) / 128) * ((N + 127) / 128) >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
     if (!out || (K > 0 && (!lhs || !rhs))) return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lhs) | reinterpret_cast<uintptr_t>(rhs)) & 1u)
         return GEMM_ERR_ALIGNMENT;

@@ -222,6 +222,17 @@ def test_plan_ragged_shape(lib):
     assert q["tiles"] == 32 * 24 and q["k_blocks"] == 33
 
 
+def test_plan_rejects_tile_counts_beyond_int(lib):
+    # 2^16 x 2^16 tiles of 128 x 128: no such output fits in memory, and the
+    # plan's tile count would overflow; refused before any launch
+    with pytest.raises(pws.GemmError) as e:
+        pws.gemm_f16_nt_plan(1 << 23, 1 << 23, 16)
+    assert e.value.status == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_f16_nt(1 << 23, 1 << 23, 16, 1 << 40, 2 << 40, 3 << 40, 4, None) == pws.GEMM_ERR_INVALID_ARG
+    p = pws.gemm_f16_nt_plan(1 << 23, 1 << 15, 16)
+    assert p["tiles"] == (1 << 15) * (1 << 6)
+
+
 def test_plan_edge_cases(lib):
     assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 2            # odd K: repacked
     assert pws.gemm_f16_nt_plan(7, 9, 3)["store"] == 1               # odd N: plain stores
