@@ -79,8 +79,9 @@ typedef uint16_t gemm_f16_t;
  * complement, i.e. the exact sum modulo 2^32).  K is cut into tiles of 16;
  * a partial last tile and partial edge tiles are zero-filled.
  *
- * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (M, N or K negative, a null pointer
- * with M*N > 0, or out overlapping an input), GEMM_ERR_ALIGNMENT (a pointer not
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (M, N or K negative or not below
+ * 2^31, ceil(M/16) * ceil(N/16) not below 2^31, a null pointer with
+ * M*N > 0, or out overlapping an input), GEMM_ERR_ALIGNMENT (a pointer not
  * 4-byte aligned), GEMM_ERR_UNSUPPORTED_ARCH or GEMM_ERR_LAUNCH.
  */
 int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const int32_t* rhs,

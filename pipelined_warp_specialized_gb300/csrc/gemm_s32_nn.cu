@@ -40,8 +40,11 @@ gemm_s32_nn_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, const i
     const int tid = threadIdx.x;
     const int tx = tid % (BN / TN);
     const int ty = tid / (BN / TN);
-    const int m0 = blockIdx.y * BM;
-    const int n0 = blockIdx.x * BN;
+    // a 1-D grid over the output tiles, row by row (a grid's y extent stops
+    // at 65535, which tall outputs would pass)
+    const int tiles_n = (N + BN - 1) / BN;
+    const int m0 = static_cast<int>(blockIdx.x / static_cast<unsigned>(tiles_n)) * BM;
+    const int n0 = static_cast<int>(blockIdx.x % static_cast<unsigned>(tiles_n)) * BN;
     const int T = (K + BK - 1) / BK;
     // launched as a programmatic dependent: the previous grid's writes first
     grid_dependency_wait();
@@ -126,10 +129,15 @@ gemm_s32_nn_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, const i
     }
 }
 
+// The grid is 1-D over the output tiles, at most 2^31 - 1 of them: with the
+// smallest (16 x 16) tile that bounds the output below 2^39 elements, more
+// than any device holds.
+inline bool too_many_tiles(int64_t M, int64_t N) { return ((M + 15) / 16) * ((N + 15) / 16) >= (1ll << 31); }
+
 template <int BM, int BN, int TM, int TN>
 cudaError_t launch_tile(int M, int N, int K, const int32_t* lhs, const int32_t* rhs, int32_t* out,
                         bool a16, bool b16, cudaStream_t stream) {
-    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>((N + BN - 1) / BN) * ((M + BM - 1) / BM)));
     // 16-byte copies need 16-byte aligned rows; otherwise one element per copy.
     const bool b_vec = b16 && BN % 4 == 0;
     if (a16 && b_vec)
@@ -151,6 +159,7 @@ extern "C" int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, 
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
+    if (s32nn::too_many_tiles(M, N)) return GEMM_ERR_INVALID_ARG;
     if (!out || (K > 0 && (!lhs || !rhs))) return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lhs) |
          reinterpret_cast<uintptr_t>(rhs)) & 3u)
@@ -213,8 +222,11 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, co
     const int tid = threadIdx.x;
     const int tx = tid % (BN / TN);
     const int ty = tid / (BN / TN);
-    const int m0 = blockIdx.y * BM;
-    const int n0 = blockIdx.x * BN;
+    // a 1-D grid over the output tiles, row by row (a grid's y extent stops
+    // at 65535, which tall outputs would pass)
+    const int tiles_n = (N + BN - 1) / BN;
+    const int m0 = static_cast<int>(blockIdx.x / static_cast<unsigned>(tiles_n)) * BM;
+    const int n0 = static_cast<int>(blockIdx.x % static_cast<unsigned>(tiles_n)) * BN;
     const int T = (K + BK - 1) / BK;
     // launched as a programmatic dependent: the previous grid's writes first
     grid_dependency_wait();
@@ -297,7 +309,7 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, co
 template <int BM, int BN, int TM, int TN, int CBYTES, int S>
 cudaError_t launch_ring_s(int M, int N, int K, const int32_t* lhs, const int32_t* rhs, int32_t* out, int device,
                           cudaStream_t stream) {
-    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
+    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>((N + BN - 1) / BN) * ((M + BM - 1) / BM)));
     constexpr size_t smem = static_cast<size_t>(S) * (BM * (BK + APAD) + BK * BN) * sizeof(int32_t);
     auto k = gemm_s32_nn_ring_kernel<BM, BN, TM, TN, CBYTES, S>;
     static std::atomic<bool> configured[64] = {};       // concurrent first calls store the same value
@@ -339,6 +351,7 @@ extern "C" int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* 
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31)) return GEMM_ERR_INVALID_ARG;
     if (stages < 2 || stages > 6) return GEMM_ERR_UNSUPPORTED_STAGES;
     if (M == 0 || N == 0) return GEMM_OK;
+    if (s32nn::too_many_tiles(M, N)) return GEMM_ERR_INVALID_ARG;
     if (!out || (K > 0 && (!lhs || !rhs))) return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(lhs) |
          reinterpret_cast<uintptr_t>(rhs)) & 3u)

@@ -231,6 +231,9 @@ def test_plan_rejects_tile_counts_beyond_int(lib):
     assert lib.gemm_f16_nt(1 << 23, 1 << 23, 16, 1 << 40, 2 << 40, 3 << 40, 4, None) == pws.GEMM_ERR_INVALID_ARG
     p = pws.gemm_f16_nt_plan(1 << 23, 1 << 15, 16)
     assert p["tiles"] == (1 << 15) * (1 << 6)
+    # the s32 calls number their (at smallest 16 x 16) tiles in a 1-D grid
+    assert lib.gemm_s32_nn(1 << 20, 1 << 20, 4, 1 << 40, 2 << 40, 3 << 40, None) == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_s32_nn_ring(1 << 20, 1 << 20, 4, 1 << 40, 2 << 40, 3 << 40, 3, None) == pws.GEMM_ERR_INVALID_ARG
 
 
 def test_plan_edge_cases(lib):

@@ -119,6 +119,22 @@ def test_graph_capture_replays_correctly():
     assert_f16_ok(o16.cpu().numpy(), oracle.gemm_f16_nt_f64(a16, b16), K)
 
 
+@pytest.mark.parametrize("ring_stages", [None, 3])
+def test_s32_very_tall_output(ring_stages):
+    # 65 537 row tiles of 128: more than a grid's y extent (65 535) holds, so
+    # the tiles are numbered along a 1-D grid
+    M, N, K = 65536 * 128 + 77, 5, 3
+    a = inputs.ints(70, 0, (M, K))
+    b = inputs.ints(70, 1, (K, N))
+    if ring_stages is None:
+        got = run_s32(a, b)
+    else:
+        out = pws.gemm_s32_nn_ring(_dev(a), _dev(b), stages=ring_stages)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+    assert np.array_equal(got, oracle.gemm_s32_nn(a, b))
+
+
 def test_s32_wraps_on_overflow():
     M, N, K = 40, 24, 64
     a = inputs.ints(1, 0, (M, K), -2**31, 2**31 - 1)
