@@ -110,6 +110,14 @@ def _check(status: int, what: str) -> None:
         raise GemmError(status, what)
 
 
+def _same_device(name, lhs, rhs, out):
+    """Every operand must live on lhs's device: the call launches there, and a
+    pointer into another GPU's memory is not valid on it."""
+    devs = {t.device for t in (lhs, rhs, out) if t is not None}
+    if len(devs) > 1:
+        raise ValueError(f"{name}: lhs, rhs and out must be on one device, got {sorted(map(str, devs))}")
+
+
 def gemm_s32_nn(lhs, rhs, out=None, stream=None):
     """out[M,N] = lhs[M,K] @ rhs[K,N] over int32 (wrapping), on lhs's device."""
     import torch
@@ -119,6 +127,7 @@ def gemm_s32_nn(lhs, rhs, out=None, stream=None):
         raise ValueError(f"shapes {tuple(lhs.shape)} x {tuple(rhs.shape)} do not form [M,K] x [K,N]")
     if not (lhs.is_cuda and rhs.is_cuda) or not lhs.is_contiguous() or not rhs.is_contiguous():
         raise ValueError("gemm_s32_nn takes contiguous CUDA tensors")
+    _same_device("gemm_s32_nn", lhs, rhs, out)
     M, K = lhs.shape
     N = rhs.shape[1]
     if out is None:
@@ -140,6 +149,7 @@ def gemm_s32_nn_ring(lhs, rhs, out=None, stages: int = 4, stream=None):
         raise ValueError(f"shapes {tuple(lhs.shape)} x {tuple(rhs.shape)} do not form [M,K] x [K,N]")
     if not (lhs.is_cuda and rhs.is_cuda) or not lhs.is_contiguous() or not rhs.is_contiguous():
         raise ValueError("gemm_s32_nn_ring takes contiguous CUDA tensors")
+    _same_device("gemm_s32_nn_ring", lhs, rhs, out)
     M, K = lhs.shape
     N = rhs.shape[1]
     if out is None:
@@ -161,6 +171,7 @@ def gemm_f16_nt(lhs, rhs, out=None, stages: int = 4, stream=None):
         raise ValueError(f"shapes {tuple(lhs.shape)} x {tuple(rhs.shape)} do not form [M,K] x [N,K]")
     if not (lhs.is_cuda and rhs.is_cuda) or not lhs.is_contiguous() or not rhs.is_contiguous():
         raise ValueError("gemm_f16_nt takes contiguous CUDA tensors")
+    _same_device("gemm_f16_nt", lhs, rhs, out)
     M, K = lhs.shape
     N = rhs.shape[0]
     if out is None:
@@ -190,6 +201,7 @@ def gemm_f16_nt_noalloc(lhs, rhs, out=None, stages: int = 4, stream=None):
         raise ValueError(f"shapes {tuple(lhs.shape)} x {tuple(rhs.shape)} do not form [M,K] x [N,K]")
     if not (lhs.is_cuda and rhs.is_cuda) or not lhs.is_contiguous() or not rhs.is_contiguous():
         raise ValueError("gemm_f16_nt_noalloc takes contiguous CUDA tensors")
+    _same_device("gemm_f16_nt_noalloc", lhs, rhs, out)
     M, K = lhs.shape
     N = rhs.shape[0]
     if out is None:

@@ -40,6 +40,34 @@ def test_binding_constants_match_the_header():
     assert all(f and f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)
 
 
+def test_binding_refuses_operands_on_different_devices():
+    # stand-ins for CUDA tensors (no GPU here): the wrappers must refuse
+    # before any launch when the operands sit on different devices
+    torch = pytest.importorskip("torch")
+
+    class Stub:
+        def __init__(self, shape, dtype, device):
+            self.shape, self.dtype, self.device, self.is_cuda = tuple(shape), dtype, torch.device(device), True
+
+        def dim(self):
+            return len(self.shape)
+
+        def is_contiguous(self):
+            return True
+
+    f16, s32 = torch.float16, torch.int32
+    cases = [
+        (pws.gemm_f16_nt, Stub((4, 8), f16, "cuda:0"), Stub((5, 8), f16, "cuda:1"), None),
+        (pws.gemm_f16_nt, Stub((4, 8), f16, "cuda:0"), Stub((5, 8), f16, "cuda:0"), Stub((4, 5), f16, "cuda:1")),
+        (pws.gemm_f16_nt_noalloc, Stub((4, 8), f16, "cuda:1"), Stub((5, 8), f16, "cuda:0"), None),
+        (pws.gemm_s32_nn, Stub((4, 8), s32, "cuda:0"), Stub((8, 5), s32, "cuda:1"), None),
+        (pws.gemm_s32_nn_ring, Stub((4, 8), s32, "cuda:0"), Stub((8, 5), s32, "cuda:0"), Stub((4, 5), s32, "cuda:2")),
+    ]
+    for fn, a, b, out in cases:
+        with pytest.raises(ValueError, match="one device"):
+            fn(a, b, out=out)
+
+
 def test_status_strings(lib):
     for code, name in [(0, "GEMM_OK"), (1, "GEMM_ERR_INVALID_ARG"), (2, "GEMM_ERR_ALIGNMENT"),
                        (3, "GEMM_ERR_UNSUPPORTED_STAGES"), (4, "GEMM_ERR_UNSUPPORTED_ARCH"),
