@@ -468,12 +468,13 @@ def test_f16_repack_scratch_is_stream_ordered():
 
 
 def test_concurrent_gemms_on_four_streams():
-    # independent f16 GEMMs (single-CTA, 256x256 and wide pair tiles, S = 1..4)
-    # and s32 GEMMs issued round-robin on four streams forked from one, first
-    # eagerly, then captured as one fork/join graph and replayed
+    # independent f16 GEMMs (single-CTA, 256x256 and wide pair tiles, S = 1..4,
+    # and two K splits, whose clusters run side by side) and s32 GEMMs issued
+    # round-robin on four streams forked from one, first eagerly, then
+    # captured as one fork/join graph and replayed
     f16_cases = []
     for i, (M, N, K) in enumerate([(300, 260, 200), (1024, 1024, 256), (4096, 4096, 64), (2304, 4608, 128),
-                                   (700, 1100, 320)]):
+                                   (700, 1100, 320), (260, 300, 2048), (129, 520, 2500)]):
         a = inputs.uniform_f16(70 + i, 0, (M, K))
         b = inputs.uniform_f16(70 + i, 1, (N, K))
         f16_cases.append((_dev(a), _dev(b), oracle.gemm_f16_nt_f64(a, b), K,
