@@ -49,3 +49,23 @@ def test_two_gloo_ranks_take_the_max_time():
 def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.25, 1, "cpu") == 3.25
+
+
+def test_reference_arm_prints_one_contract_line():
+    # bench.py --impl reference times the CPU oracle (the reference arm) and
+    # prints one JSON line with the contract's keys; on a tiny shape here
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
+                        "--shape", "64,48,80"], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert (d["steps"], d["warmup"], d["n_gpus"]) == (2, 3, 1)
+    assert d["config"]["M"] == 64 and d["config"]["N"] == 48 and d["config"]["K"] == 80
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
