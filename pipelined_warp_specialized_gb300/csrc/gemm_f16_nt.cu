@@ -748,8 +748,9 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         // quarter: 16-byte unit u (fp32 columns 4u..4u+3) of lane l's row at
         // u * 512 + l * 16, so one unit of all 32 rows is one contiguous
         // 512-byte block (conflict-free, one request per warp).  Measured on
-        // GB300: the owner reading the sums from the peer instead cost about
-        // 2 us more per tile, each remote round trip exposed.
+        // GB300: the owner reading the sums from the peer's shared memory
+        // instead cost 0.35-0.5 us more per tile (each remote round trip
+        // exposed), and 2-4 us more with a 512-byte row per lane.
         const bool sender = kpair && static_cast<uint32_t>(q >> 1) != krank;
         const uint32_t recv_lane = sEPI + static_cast<uint32_t>(q & 1) * (32u * 512u) + static_cast<uint32_t>(lane) * 16u;
         const uint32_t push_lane = sender ? mapa_shared(recv_lane, krank ^ 1u) : 0u;
