@@ -360,6 +360,25 @@ def concurrency_configs(pws, torch, G=16, stream_counts=(1, 2, 4, 8)):
     return out
 
 
+def sweep_model(res, plan, pairs):
+    """The pipeline cost model (TileLang tutorial ch.22, section 1.1) fitted
+    to the sweep's S = 1 and S = 4 points (the same wide tile), and its
+    prediction for S = 2 and 3 beside the measurement."""
+    from pipelined_warp_specialized_gb300 import cost_model
+    if not all(f"S{s}" in res and res[f"S{s}"]["tile"] == res["S1"]["tile"] for s in (1, 2, 3, 4)):
+        return None
+    units = plan["tiles"]                       # wide tiles, one wave of `pairs` CTA pairs at a time
+    blocks = -(-units // pairs) * plan["k_blocks"]     # the busiest pair's K blocks
+    t1, t4 = res["S1"]["us"], res["S4"]["us"]
+    c, latency = cost_model.fit(blocks, t1, t4)
+    pred = cost_model.predict_sweep(blocks, t1, t4, (2, 3))
+    return {"fit": "c and L per K block from S = 1 (B (L + c)) and S = 4 (B c), B = the busiest CTA pair's blocks",
+            "blocks": blocks, "c_us": round(c, 4), "L_us": round(latency, 4),
+            "saturation_S": round(cost_model.saturation_stages(c, latency), 2),
+            **{f"S{s}": {"predicted_us": round(pred[s], 1), "measured_us": res[f"S{s}"]["us"],
+                         "measured_over_predicted": round(res[f"S{s}"]["us"] / pred[s], 3)} for s in (2, 3)}}
+
+
 def extra_configs(pws, torch, stream):
     """Kernel-only timings of every workload (inputs resident)."""
     out = {}
@@ -406,6 +425,9 @@ def extra_configs(pws, torch, stream):
                                               else "0.25 s warm-up, then 0.25 s of back-to-back launches")
             finally:
                 pws.gemm_set_debug_flags(0)
+            if name == "f16_nt_8192" and not suffix:
+                pairs = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count // 2
+                res["model"] = sweep_model(res, plan, pairs)
             out[name + ("/" + suffix if suffix else "")] = res
         del a, b, c
     out.update(concurrency_configs(pws, torch))
