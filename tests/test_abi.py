@@ -190,6 +190,25 @@ def test_plan_wave_count_rules(lib):
         assert tile(8192, 8192, 8192, s) == (256, 512)
 
 
+def test_plan_sum_order_never_depends_on_stages(lib):
+    # Results are bitwise identical across S because the choices that change
+    # the summation (the K split) or could (single CTA vs pair) read the shape
+    # only.  Checked over a grid of shapes around every threshold of the
+    # rules: tile-count edges, the 32-block K-split edge, ragged sizes.
+    pws.gemm_set_debug_flags(0)
+    dims = [1, 64, 129, 256, 300, 640, 1000, 1024, 1152, 1216, 1536, 2048, 2304, 2560, 3072, 4096, 9728, 20000]
+    ks = [1, 64, 200, 1984, 1985, 2048, 4100, 8192]
+    for M in dims:
+        for N in dims:
+            for K in ks:
+                plans = [pws.gemm_f16_nt_plan(M, N, K, stages=s) for s in range(1, 7)]
+                assert len({(p["cta_group"], p["k_split"], p["bk"]) for p in plans}) == 1, (M, N, K)
+                for s, p in enumerate(plans, start=1):
+                    assert p["bn"] != 512 or s <= 4, (M, N, K, s)            # the wide tile needs <= 4 slots
+                    assert p["k_split"] == 1 or p["cta_group"] == 1, (M, N, K)
+                    assert p["k_split"] == 1 or p["k_blocks"] >= 32, (M, N, K)
+
+
 def test_smoke_cases_plan_the_paths_they_check(lib):
     # smoke() runs on the GPU only at round end; its plan expectations are
     # host logic and are checked here first

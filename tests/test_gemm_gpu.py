@@ -175,6 +175,21 @@ def test_f16_stage_counts_bitwise_identical(flags):
     assert_f16_ok(outs[0], oracle.gemm_f16_nt_f64(a, b), K)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (2560, 2560, 256),      # wide tile for S <= 2, 256 x 256 for S >= 3: the same bits
+    (2048, 2048, 512),      # the pair tile by wave count (64 pair tiles against 256 single)
+    (1024, 1152, 2100),     # the K split on repacked operands
+])
+def test_f16_stage_counts_bitwise_identical_where_the_plan_changes(M, N, K):
+    a = inputs.uniform_f16(M + K, 0, (M, K))
+    b = inputs.uniform_f16(M + K, 1, (N, K))
+    tiles = {(p["bm"], p["bn"], p["k_split"]) for p in (pws.gemm_f16_nt_plan(M, N, K, stages=s) for s in range(1, 7))}
+    outs = [run_f16(a, b, s) for s in range(1, 7)]
+    for s in range(1, 6):
+        assert np.array_equal(outs[s].view(np.uint16), outs[0].view(np.uint16)), f"S={s + 1} differs ({tiles})"
+    assert_f16_ok(outs[0], oracle.gemm_f16_nt_f64(a, b), K)
+
+
 @pytest.mark.parametrize("M,N,K,flags", [
     (1, 1, 1, 0), (1, 1, 8, 0), (5, 3, 64, 0), (128, 128, 64, 0), (129, 130, 72, 0),
     (260, 300, 136, pws.GEMM_DEBUG_FORCE_PAIR_TILE),      # second pair row: the peer CTA is all padding
