@@ -261,6 +261,10 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *   GEMM_DEBUG_FORCE_KSPLIT        : split K wherever the single-CTA tile is
  *       used and there are at least 2 K blocks, however many tiles there are
  *       (clusters beyond those that fit at once run as the GPU frees SMs).
+ *   GEMM_DEBUG_SKIP_KSPLIT_SEND    : in the K split, the warps that send
+ *       their partial sums to the peer CTA send nothing and never signal it;
+ *       used to test that the owners' wait for them ends in GEMM_ERR_TIMEOUT
+ *       while the rest of the cluster finishes normally.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -274,7 +278,8 @@ enum {
     GEMM_DEBUG_FORCE_WIDE_TILE = 128u,
     GEMM_DEBUG_SKIP_ACC_SEED = 256u,
     GEMM_DEBUG_NO_KSPLIT = 512u,
-    GEMM_DEBUG_FORCE_KSPLIT = 1024u
+    GEMM_DEBUG_FORCE_KSPLIT = 1024u,
+    GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048u
 };
 int gemm_set_debug_flags(unsigned flags);
 

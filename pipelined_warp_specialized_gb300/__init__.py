@@ -40,6 +40,7 @@ GEMM_DEBUG_FORCE_WIDE_TILE = 128
 GEMM_DEBUG_SKIP_ACC_SEED = 256
 GEMM_DEBUG_NO_KSPLIT = 512
 GEMM_DEBUG_FORCE_KSPLIT = 1024
+GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048
 
 _lib = None
 

@@ -918,7 +918,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + i * SH::ACC_COLS;
 #pragma unroll 1
-            for (int c = 0; c < SH::ACC_COLS / 64; ++c) {
+            for (int c = 0; c < (p.flags & GEMM_DEBUG_SKIP_KSPLIT_SEND ? 0 : SH::ACC_COLS / 64); ++c) {
                 uint32_t v0[32], v1[32];
                 tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 64), v0);
                 tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 64 + 32), v1);
@@ -934,7 +934,8 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             }
             tc_fence_before_sync();
             __syncwarp();
-            mbar_arrive_cluster(mapa_shared(bRECV + 8 * static_cast<uint32_t>(q & 1), krank ^ 1u));
+            if (!(p.flags & GEMM_DEBUG_SKIP_KSPLIT_SEND))
+                mbar_arrive_cluster(mapa_shared(bRECV + 8 * static_cast<uint32_t>(q & 1), krank ^ 1u));
             if (lane == 0) mbar_arrive(bTEMPTY + 8 * i);
             return true;
         };

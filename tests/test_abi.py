@@ -123,7 +123,7 @@ def test_s32_ring_argument_checks_return_before_launch(lib, args, want):
 
 
 def test_debug_flags_and_timeout_setters(lib):
-    assert lib.gemm_set_debug_flags(1 << 11) == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_debug_flags(1 << 12) == pws.GEMM_ERR_INVALID_ARG
     assert lib.gemm_set_debug_flags(0) == pws.GEMM_OK
     assert lib.gemm_set_wait_timeout_ns(0) == pws.GEMM_OK
 

@@ -66,3 +66,43 @@ def test_missing_seed_times_out_and_context_survives(seed_flag, extra, N):
     res = oracle.check_f16(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_np, b_np), K)
     assert res["ok"], res
     assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("extra", [0, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER], ids=["tma", "copy"])
+def test_k_split_missing_partial_sums_time_out(extra):
+    # In the K split the owner of each lane quarter waits for its peer CTA's
+    # partial sums.  With the senders silenced, that wait alone runs out (0.2
+    # s): every other role of both CTAs completes normally, both CTAs meet at
+    # the final cluster barrier, the call reports GEMM_ERR_TIMEOUT, and the
+    # next call is correct.
+    M, N, K = 256, 256, 256
+    a_np = inputs.uniform_f16(3, 0, (M, K))
+    b_np = inputs.uniform_f16(3, 1, (N, K))
+    a = torch.from_numpy(a_np).cuda()
+    b = torch.from_numpy(b_np).cuda()
+    flags = pws.GEMM_DEBUG_FORCE_KSPLIT | extra
+    pws.gemm_set_debug_flags(flags)
+    try:
+        assert pws.gemm_f16_nt_plan(M, N, K, stages=2)["k_split"] == 2
+    finally:
+        pws.gemm_set_debug_flags(0)
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    pws.gemm_set_wait_timeout_ns(200_000_000)
+    pws.gemm_set_debug_flags(flags | pws.GEMM_DEBUG_SKIP_KSPLIT_SEND)
+    try:
+        pws.gemm_f16_nt(a, b, stages=2)
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_ERR_TIMEOUT
+        assert pws.gemm_device_status() == pws.GEMM_OK
+    finally:
+        pws.gemm_set_debug_flags(0)
+        pws.gemm_set_wait_timeout_ns(0)
+    pws.gemm_set_debug_flags(flags)
+    try:
+        out = pws.gemm_f16_nt(a, b, stages=2)
+        torch.cuda.synchronize()
+    finally:
+        pws.gemm_set_debug_flags(0)
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    res = oracle.check_f16(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_np, b_np), K)
+    assert res["ok"], res
