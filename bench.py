@@ -2,7 +2,7 @@
 """Benchmark of the pipelined, warp-specialized GEMM library on GB300.
 
 One step = one f16 NT GEMM over the headline workload (default 8192^3 with
-S = 6 ring slots, lhs [M,K] and rhs [N,K] f16 uniform in [-1,1] from seed 5,
+S = 4 ring slots, lhs [M,K] and rhs [N,K] f16 uniform in [-1,1] from seed 5,
 fp32 accumulate, f16 out), launched through the C ABI.  The inputs stay resident in HBM during
 the timed region and are larger than the 129 MB L2 (256 MB of operands), so
 no L2 flush is needed between steps.
@@ -17,12 +17,16 @@ Prints ONE JSON line (rank 0):
   roofline              -- the GEMM kernel's achieved TFLOP/s against the
                            measured dense 16-bit tensor peak
   cpu_baseline          -- the CPU oracle timed on a bounded sample of the
-                           same workload on this host's cores
+                           same workload on this host's cores, and whole on
+                           each smaller workload (per_config; 1024^3 also on
+                           one thread)
   clocks                -- nvidia-smi samples taken during the timed region
   configs               -- the other workloads (kernel-only timings): s32 NN
                            128x256x256, f16 NT 1024^3 S=2, 4096^3 S=4, the
-                           ragged 4000x3000x2050 S=3 and the 8192^3 S=1..6 sweep,
-                           and 16 independent 1024^3 f16 / s32 GEMMs issued
+                           ragged 4000x3000x2050 S=3 and the 8192^3 S=1..6 sweep
+                           (each point after 0.25 s of warm-up, and the pipeline
+                           cost model fitted to it), and 16 independent
+                           1024^3 f16 / s32 GEMMs issued
                            on 1, 2, 4 or 8 streams (host concurrency)
                            and per-launch median / p10 / p90 at 4096^3, 8192^3
 
