@@ -162,8 +162,9 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  * rounding of the same exact sum than the one-pass tiles give.  The choice
  * depends on M, N and K only, so the result is still the same for every S.
  *
- * The kernel is persistent: a grid of as many CTA groups as fit on the GPU
- * strides over the output tiles.  When the tile count leaves a last, partial
+ * The kernel is persistent (the K split aside, which runs one cluster per
+ * tile): a grid of as many CTA groups as fit on the GPU strides over the
+ * output tiles.  When the tile count leaves a last, partial
  * wave that fills at most half of the grid, each tile of that wave runs as
  * two units, its left and right halves of columns, on the wave's otherwise
  * idle CTA groups.  Each half runs the whole K loop, so no partial sums are
