@@ -400,9 +400,12 @@ def test_f16_repack_every_row_alignment(offset):
         assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b_t.cpu().numpy()), K)
 
 
-@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER])
+@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER,
+                                   pws.GEMM_DEBUG_FORCE_KSPLIT,
+                                   pws.GEMM_DEBUG_FORCE_KSPLIT | pws.GEMM_DEBUG_FORCE_COPY_PRODUCER])
 def test_f16_closed_forms_bit_exact(flags):
     # rank one with dyadic values: every sum is K * a_m * b_n, exact in fp32 and in f16
+    # (with the K split each half's sum is exact too, so the added halves must be)
     K = 1024
     a = np.array([1.0, -1.0, 0.5, -0.5] * 75, np.float16)            # M = 300
     b = np.array([0.5, 1.0, -1.0, -0.5, 1.0] * 52, np.float16)       # N = 260
