@@ -194,11 +194,15 @@ int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const ge
  * front, and code that must not enter an allocator (which may synchronize or
  * fail at a point the caller cannot handle).
  *   - Scratch needed: round256(M*Kp*2) + round256(N*Kp*2) bytes, Kp = K
- *     rounded up to a multiple of 8.  Above 32 MiB (33554432 bytes) the call
- *     returns GEMM_ERR_INVALID_ARG without launching anything.  Operands the
- *     accelerator can address directly need no scratch and have no limit.
+ *     rounded up to a multiple of 8.  Operands that would need more than the
+ *     32 MiB (33554432 bytes) are read in place by the asynchronous-copy
+ *     producer instead, which needs no scratch (slower, same result bits).
+ *     Operands the accelerator can address directly need no scratch at all.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset (or any other replacement of the device's primary
+ *     context) this entry point must not be called again in that process.
  *   - All calls share the one array.  Calls that can overlap on the GPU (on
  *     streams with no ordering between them) race on it: order them.  The
  *     array keeps the last call's contents; each call overwrites every byte

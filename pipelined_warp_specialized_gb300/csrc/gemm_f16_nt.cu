@@ -62,7 +62,10 @@
 // Every wait is bounded (wait_timeout_ns); a role that gives up records a
 // timeout in the library's status word, raises a CTA-local abort flag that
 // the other roles poll, and every role then runs the common exit path, so
-// the kernel always returns.
+// the kernel always returns.  Waits that last about one K block (the ring's)
+// count the limit from their start; the waits that last a whole K loop (a
+// finished accumulator, the K split's partial sums) count it from the last K
+// block the producer issued, so they end on a stall, not on a long K.
 #include <cstdint>
 #include <algorithm>
 #include <atomic>
@@ -166,7 +169,8 @@ struct Layout {
     static constexpr int RECV = DRAIN + 8;                   // K split: a peer warp's partial rows are staged (x2)
     static constexpr int TMEM_SLOT = RECV + 16;
     static constexpr int ABORT = TMEM_SLOT + 4;
-    static constexpr int END = ABORT + 4;
+    static constexpr int PROGRESS = ABORT + 4;               // K blocks this CTA's producer has issued
+    static constexpr int END = PROGRESS + 4;
     static constexpr int BYTES = END + 1024;                // + alignment slack
     // at least ~half the SM's shared memory so only one CTA is resident per SM
     // (each CTA owns up to all 512 tensor-memory columns)
@@ -237,6 +241,14 @@ struct Waiter {
         return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     }
 
+    __device__ __forceinline__ bool give_up() const {
+        *abort = 1u;
+        atomicOr(status, kStatusTimeout | role);
+        return false;
+    }
+
+    // A wait that lasts about one K block (the ring's, the accumulator
+    // hand-over's): the limit counts from the start of the wait.
     template <bool CLUSTER_SCOPE = false>
     __device__ bool wait(uint32_t bar, uint32_t parity) const {
         if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
@@ -244,10 +256,33 @@ struct Waiter {
         for (;;) {
             if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) {
-                *abort = 1u;
-                atomicOr(status, kStatusTimeout | role);
-                return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return give_up();
+        }
+    }
+
+    // A wait that legitimately lasts a whole K loop: the epilogue's wait for
+    // a finished accumulator, and the K split's wait for the peer's partial
+    // sums.  The limit counts from the last change of the progress counter
+    // that the producer of the CTA being waited for bumps once per K block
+    // (`remote`: the counter lives in the other CTA of the cluster), so such
+    // a wait gives up on a stall -- no K block issued for the whole limit --
+    // and never on a long but live loop.  After the producer's last block the
+    // wait still has to cover at most S blocks of multiplies and a drain.
+    template <bool CLUSTER_SCOPE = false>
+    __device__ bool wait_progress(uint32_t bar, uint32_t parity, uint32_t progress, bool remote) const {
+        if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
+        uint64_t t0 = globaltimer_ns();
+        uint32_t seen = remote ? ld_relaxed_cluster_u32(progress) : ld_volatile_shared_u32(progress);
+        for (;;) {
+            if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
+            if (*abort) return false;
+            const uint32_t now_seen = remote ? ld_relaxed_cluster_u32(progress) : ld_volatile_shared_u32(progress);
+            const uint64_t now = globaltimer_ns();
+            if (now_seen != seen) {
+                seen = now_seen;
+                t0 = now;
+            } else if (now - t0 > timeout_ns) {
+                return give_up();
             }
         }
     }
@@ -322,7 +357,8 @@ __device__ __forceinline__ void copy_strip(uint32_t slot, const __half* base, in
 // k - S + GROUP - 1.
 template <int G, int S>
 __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB, uint32_t bFULL,
-                              uint32_t bEMPTY, int cluster_id, int num_clusters, int kb0, int kb1, int lane) {
+                              uint32_t bEMPTY, uint32_t progress, int cluster_id, int num_clusters, int kb0, int kb1,
+                              int lane) {
     constexpr int LAG = S - (S >= 6 ? 2 : 1);
     const int t = threadIdx.x;                   // 0 .. COPY_THREADS - 1
     uint32_t stage = 0, phase = 0, issued = 0, signalled = 0;
@@ -340,6 +376,7 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
             copy_strip<G>(sB + stage * B_SLOT, p.rhs, p.N, tn * BN_CTA, p.K, kb * BK, t);
             cp_async_commit();
             ++issued;
+            if (t == 0) st_volatile_shared_u32(progress, issued);
             if (issued - signalled > static_cast<uint32_t>(LAG)) {
                 cp_async_wait_group<LAG>();
                 fence_proxy_async_smem();
@@ -397,6 +434,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const uint32_t bRECV = base + L::RECV;
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + L::ABORT);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::TMEM_SLOT);
+    const uint32_t sPROGRESS = base + L::PROGRESS;
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
@@ -414,6 +452,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         // K split: the 32 lanes of the peer's warp for lane quarter 2*krank + j
         for (int j = 0; j < 2; ++j) mbar_init(bRECV + 8 * j, 32);
         *abort_flag = 0u;
+        *reinterpret_cast<volatile uint32_t*>(gbase + L::PROGRESS) = 0u;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0 && p.producer == kProducerTma) {
@@ -486,6 +525,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                                                  full_leader + 8 * stage);
                         }
                         ++issued;
+                        st_volatile_shared_u32(sPROGRESS, issued);
                         if (++stage == S) { stage = 0; phase ^= 1u; }
                     }
                 }
@@ -511,11 +551,11 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             // cp.async producer (single CTA only): COPY_WARPS warps fill the swizzled slot
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
             if (p.copy_bytes == 8)
-                copy_producer<8, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, kb0, kb1, lane);
+                copy_producer<8, S>(p, W, sA, sB, bFULL, bEMPTY, sPROGRESS, cluster_id, num_clusters, kb0, kb1, lane);
             else if (p.copy_bytes == 4)
-                copy_producer<4, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, kb0, kb1, lane);
+                copy_producer<4, S>(p, W, sA, sB, bFULL, bEMPTY, sPROGRESS, cluster_id, num_clusters, kb0, kb1, lane);
             else
-                copy_producer<2, S>(p, W, sA, sB, bFULL, bEMPTY, cluster_id, num_clusters, kb0, kb1, lane);
+                copy_producer<2, S>(p, W, sA, sB, bFULL, bEMPTY, sPROGRESS, cluster_id, num_clusters, kb0, kb1, lane);
         }
         __syncwarp();
     } else if (warp == mma_warp) {
@@ -755,6 +795,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const uint32_t recv_lane = sEPI + static_cast<uint32_t>(q & 1) * (32u * 512u) + static_cast<uint32_t>(lane) * 16u;
         const uint32_t push_lane = sender ? mapa_shared(recv_lane, krank ^ 1u) : 0u;
         const uint32_t peer_sums = kpair && !sender ? recv_lane : 0u;
+        const uint32_t peer_progress = kpair ? mapa_shared(sPROGRESS, krank ^ 1u) : 0u;
         static_assert(SH::ACC_COLS / 4 * 512 <= 32 * 512 || CG == 2, "a received quarter holds the single tile's 128 fp32 columns");
         static_assert(2 * 32 * 512 == EPI_BYTES, "the staging area holds the two received quarters");
         static_assert(EPI_WARPS * 2 * EPI_BUF <= A_SLOT + B_SLOT, "the owners' output staging fits in the smallest ring");
@@ -831,7 +872,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         // tensor-memory load and the rounding together).
         auto drain = [&](uint32_t i, uint32_t par, uint32_t acc_col0, int ncols, int row0, int col_base) {
             bool got = true;
-            if (lane == 0) got = W.wait(bTFULL + 8 * i, par);
+            if (lane == 0) got = W.wait_progress(bTFULL + 8 * i, par, sPROGRESS, false);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) return false;
             tc_fence_after_sync();
@@ -912,7 +953,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         // if the wait gave up.
         auto send = [&](uint32_t i, uint32_t par) {
             bool got = true;
-            if (lane == 0) got = W.wait(bTFULL + 8 * i, par);
+            if (lane == 0) got = W.wait_progress(bTFULL + 8 * i, par, sPROGRESS, false);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) return false;
             tc_fence_after_sync();
@@ -959,8 +1000,11 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     }
                     // the owner: every lane waits (its own acquire orders its
                     // reads of the peer's rows), and the warp goes on only if
-                    // all lanes' waits completed
-                    bool got = W.template wait<true>(bRECV + 8 * static_cast<uint32_t>(q & 1), 0);
+                    // all lanes' waits completed.  The peer's sums come after
+                    // the peer's whole K loop: the limit counts from the last
+                    // K block the peer's producer issued.
+                    bool got = W.template wait_progress<true>(bRECV + 8 * static_cast<uint32_t>(q & 1), 0,
+                                                              peer_progress, true);
                     if (!__all_sync(0xffffffffu, got)) break;
                 }
                 if (!drain(b, aph, b * SH::ACC_COLS, ncols, row0, col_base)) break;
@@ -1393,6 +1437,87 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
     return GEMM_OK;
 }
 
+namespace pws {
+namespace f16nt {
+
+// K == 0: the empty sum, zeros.
+int zero_output(gemm_f16_t* out, int64_t M, int64_t N, const DeviceInfo& info, cudaStream_t stream) {
+    const int64_t n = M * N;
+    int blocks = static_cast<int>((n + 255) / 256);
+    if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
+    return launch_pdl(zero_fill_u16, dim3(blocks), dim3(256), 0, stream, reinterpret_cast<unsigned short*>(out), n) ==
+                   cudaSuccess
+               ? GEMM_OK
+               : GEMM_ERR_LAUNCH;
+}
+
+// Encodes the tensor maps, fills the kernel parameters and launches the GEMM
+// of plan `pl`.  The TMA producer reads the operands at a_src / b_src with
+// rows `ld` elements apart (the caller's own, or a repacked copy); the
+// copy producer reads lhs / rhs in place.
+int run_plan(const Plan& pl, const DeviceInfo& info, int64_t M, int64_t N, int64_t K, const void* lhs,
+             const void* rhs, void* out, const void* a_src, const void* b_src, int64_t ld, int stages, unsigned flags,
+             cudaStream_t stream) {
+    CUtensorMap ta, tb, tbh, tc;
+    memset(&ta, 0, sizeof(ta));
+    memset(&tb, 0, sizeof(tb));
+    memset(&tbh, 0, sizeof(tbh));
+    memset(&tc, 0, sizeof(tc));
+    if (pl.producer == kProducerTma) {
+        if (!encode_tmap_f16_2d(&ta, a_src, K, M, ld * 2, BK, BM_CTA) ||
+            !encode_tmap_f16_2d(&tb, b_src, K, N, ld * 2, BK, BN_CTA))
+            return GEMM_ERR_LAUNCH;
+    }
+    if (pl.store == kStoreTma) {
+        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return GEMM_ERR_LAUNCH;
+    }
+    Params p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = pl.num_kb;
+    p.tiles_m = pl.tiles_m;
+    p.tiles_n = pl.tiles_n;
+    p.num_tiles = pl.num_tiles;
+    p.producer = pl.producer;
+    p.copy_bytes = pl.copy_bytes;
+    p.store = pl.store;
+    p.flags = flags;
+    p.timeout_ns = wait_timeout_ns();
+    p.lhs = static_cast<const __half*>(lhs);
+    p.rhs = static_cast<const __half*>(rhs);
+    p.out = static_cast<__half*>(out);
+    p.status = info.status;
+    p.full_units = pl.num_tiles;
+    p.split = 0;
+    p.total_units = pl.num_tiles;
+    p.ksplit = pl.ksplit;
+
+    // Tail split: when the tiles leave a last, partial wave of the persistent
+    // grid (or fewer tiles than the grid) and twice that many units still
+    // fit in one wave, each of those tiles runs as two half-width units on the
+    // wave's otherwise idle CTA groups.  Only the TMA producer supports it
+    // (the 256 x 256 and 128 x 128 tiles need a 64-row B box; a half of the
+    // wide tile is one ordinary box).  Each output element is still one
+    // in-order K sum; the decision depends on the shape and the device, never
+    // on S.
+    const int cap = capacity_of(pl, stages, info);
+    if (cap <= 0) return GEMM_ERR_LAUNCH;
+    const int waves = pl.num_tiles / cap;
+    const int tail = pl.num_tiles - waves * cap;
+    if (pl.producer == kProducerTma && pl.ksplit == 1 && tail > 0 && 2 * tail <= cap &&
+        !(flags & GEMM_DEBUG_NO_SPLIT)) {
+        if (pl.nw == 1 && !encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return GEMM_ERR_LAUNCH;
+        p.full_units = waves * cap;
+        p.split = 2;
+        p.total_units = waves * cap + 2 * tail;
+    }
+    return launch_plan(stages, pl, info, ta, tb, tbh, tc, p, stream);
+}
+
+}  // namespace f16nt
+}  // namespace pws
+
 extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                            gemm_f16_t* out, int stages, cudaStream_t stream) {
     using namespace pws;
@@ -1403,15 +1528,7 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     DeviceInfo info;
     rc = current_device(&info);
     if (rc != GEMM_OK) return rc;
-    if (K == 0) {
-        const int64_t n = M * N;
-        int blocks = static_cast<int>((n + 255) / 256);
-        if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
-        return launch_pdl(zero_fill_u16, dim3(blocks), dim3(256), 0, stream, reinterpret_cast<unsigned short*>(out), n) ==
-                       cudaSuccess
-                   ? GEMM_OK
-                   : GEMM_ERR_LAUNCH;
-    }
+    if (K == 0) return zero_output(out, M, N, info, stream);
     const unsigned flags = debug_flags();
     Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
 
@@ -1441,67 +1558,9 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
             pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, false);
         }
     }
-
-    CUtensorMap ta, tb, tc;
-    memset(&ta, 0, sizeof(ta));
-    memset(&tb, 0, sizeof(tb));
-    memset(&tc, 0, sizeof(tc));
-    auto done = [&](int status) {
-        scratch_free(scratch, stream);       // stream-ordered: after the GEMM has read it
-        return status;
-    };
-    if (pl.producer == kProducerTma) {
-        if (!encode_tmap_f16_2d(&ta, a_src, K, M, ld * 2, BK, BM_CTA) ||
-            !encode_tmap_f16_2d(&tb, b_src, K, N, ld * 2, BK, BN_CTA))
-            return done(GEMM_ERR_LAUNCH);
-    }
-    if (pl.store == kStoreTma) {
-        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return done(GEMM_ERR_LAUNCH);
-    }
-    Params p;
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.num_kb = pl.num_kb;
-    p.tiles_m = pl.tiles_m;
-    p.tiles_n = pl.tiles_n;
-    p.num_tiles = pl.num_tiles;
-    p.producer = pl.producer;
-    p.copy_bytes = pl.copy_bytes;
-    p.store = pl.store;
-    p.flags = flags;
-    p.timeout_ns = wait_timeout_ns();
-    p.lhs = reinterpret_cast<const __half*>(lhs);
-    p.rhs = reinterpret_cast<const __half*>(rhs);
-    p.out = reinterpret_cast<__half*>(out);
-    p.status = info.status;
-    p.full_units = pl.num_tiles;
-    p.split = 0;
-    p.total_units = pl.num_tiles;
-    p.ksplit = pl.ksplit;
-
-    // Tail split: when the tiles leave a last, partial wave of the persistent
-    // grid (or fewer tiles than the grid) and twice that many units still
-    // fit in one wave, each of those tiles runs as two half-width units on the
-    // wave's otherwise idle CTA groups.  Only the TMA producer supports it
-    // (the 256 x 256 and 128 x 128 tiles need a 64-row B box; a half of the
-    // wide tile is one ordinary box).  Each output element is still one
-    // in-order K sum; the decision depends on the shape and the device, never
-    // on S.
-    CUtensorMap tbh;
-    memset(&tbh, 0, sizeof(tbh));
-    const int cap = capacity_of(pl, stages, info);
-    if (cap <= 0) return done(GEMM_ERR_LAUNCH);
-    const int waves = pl.num_tiles / cap;
-    const int tail = pl.num_tiles - waves * cap;
-    if (pl.producer == kProducerTma && pl.ksplit == 1 && tail > 0 && 2 * tail <= cap &&
-        !(flags & GEMM_DEBUG_NO_SPLIT)) {
-        if (pl.nw == 1 && !encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return done(GEMM_ERR_LAUNCH);
-        p.full_units = waves * cap;
-        p.split = 2;
-        p.total_units = waves * cap + 2 * tail;
-    }
-    return done(launch_plan(stages, pl, info, ta, tb, tbh, tc, p, stream));
+    rc = run_plan(pl, info, M, N, K, lhs, rhs, out, a_src, b_src, ld, stages, flags, stream);
+    scratch_free(scratch, stream);       // stream-ordered: after the GEMM has read it
+    return rc;
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -1514,6 +1573,8 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
 // point the caller cannot handle), or code that has reserved all device
 // memory up front.  gemm_f16_nt_noalloc serves them with scratch that exists
 // from the moment the library is loaded: a fixed array in device memory.
+// Operands that would need more scratch than the array holds are read in
+// place by the cp.async producer, which needs none.
 namespace pws {
 namespace f16nt {
 
@@ -1558,72 +1619,32 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     DeviceInfo info;
     rc = current_device(&info);
     if (rc != GEMM_OK) return rc;
-    if (K == 0) {
-        const int64_t n = M * N;
-        int blocks = static_cast<int>((n + 255) / 256);
-        if (blocks > 8 * info.num_sms) blocks = 8 * info.num_sms;
-        return launch_pdl(zero_fill_u16, dim3(blocks), dim3(256), 0, stream, reinterpret_cast<unsigned short*>(out), n) ==
-                       cudaSuccess
-                   ? GEMM_OK
-                   : GEMM_ERR_LAUNCH;
-    }
+    if (K == 0) return zero_output(out, M, N, info, stream);
     const unsigned flags = debug_flags();
-    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
 
     const void* a_src = lhs;
     const void* b_src = rhs;
     int64_t ld = K;
     if (pl.repack) {
         size_t b_off = 0;
-        if (repack_bytes(M, N, K, &b_off, 8) > kNoAllocScratchBytes) return GEMM_ERR_INVALID_ARG;
-        void* scratch = noalloc_scratch(info.device);
-        if (!scratch) return GEMM_ERR_LAUNCH;
-        // The repack writes every scratch byte the GEMM then reads (padding
-        // included), so nothing left over from an earlier call is ever used.
-        const int64_t Kp = (K + 7) / 8 * 8;
-        uint16_t* da = static_cast<uint16_t*>(scratch);
-        uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
-        if (launch_repack(lhs, M, rhs, N, K, Kp, Kp, da, db, stream) != cudaSuccess)
-            return GEMM_ERR_LAUNCH;
-        a_src = da;
-        b_src = db;
-        ld = Kp;
+        if (repack_bytes(M, N, K, &b_off, 8) > kNoAllocScratchBytes) {
+            // more scratch than the array holds: the producer that reads the
+            // operands in place needs none
+            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, false);
+        } else {
+            void* scratch = noalloc_scratch(info.device);
+            if (!scratch) return GEMM_ERR_LAUNCH;
+            // The repack writes every scratch byte the GEMM then reads (padding
+            // included), so nothing left over from an earlier call is ever used.
+            const int64_t Kp = (K + 7) / 8 * 8;
+            uint16_t* da = static_cast<uint16_t*>(scratch);
+            uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
+            if (launch_repack(lhs, M, rhs, N, K, Kp, Kp, da, db, stream) != cudaSuccess) return GEMM_ERR_LAUNCH;
+            a_src = da;
+            b_src = db;
+            ld = Kp;
+        }
     }
-
-    CUtensorMap ta, tb, tc;
-    memset(&ta, 0, sizeof(ta));
-    memset(&tb, 0, sizeof(tb));
-    memset(&tc, 0, sizeof(tc));
-    if (pl.producer == kProducerTma) {
-        if (!encode_tmap_f16_2d(&ta, a_src, K, M, ld * 2, BK, BM_CTA) ||
-            !encode_tmap_f16_2d(&tb, b_src, K, N, ld * 2, BK, BN_CTA))
-            return GEMM_ERR_LAUNCH;
-    }
-    if (pl.store == kStoreTma) {
-        if (!encode_tmap_f16_2d(&tc, out, N, M, N * 2, EPI_COLS, 32)) return GEMM_ERR_LAUNCH;
-    }
-    Params p;
-    p.M = static_cast<int>(M);
-    p.N = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.num_kb = pl.num_kb;
-    p.tiles_m = pl.tiles_m;
-    p.tiles_n = pl.tiles_n;
-    p.num_tiles = pl.num_tiles;
-    p.producer = pl.producer;
-    p.copy_bytes = pl.copy_bytes;
-    p.store = pl.store;
-    p.flags = flags;
-    p.timeout_ns = wait_timeout_ns();
-    p.lhs = reinterpret_cast<const __half*>(lhs);
-    p.rhs = reinterpret_cast<const __half*>(rhs);
-    p.out = reinterpret_cast<__half*>(out);
-    p.status = info.status;
-    p.full_units = pl.num_tiles;        // whole tiles only
-    p.split = 0;
-    p.total_units = pl.num_tiles;
-    p.ksplit = pl.ksplit;               // as gemm_f16_nt: the same sums
-    CUtensorMap tbh;                    // unused without the tail split
-    memset(&tbh, 0, sizeof(tbh));
-    return launch_plan(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    return run_plan(pl, info, M, N, K, lhs, rhs, out, a_src, b_src, ld, stages, flags, stream);
 }

@@ -127,6 +127,26 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
                  : "memory");
 }
 
+// A progress counter in shared memory: written by one thread, polled by
+// waiters of this CTA (local) or of the other CTA of the cluster (remote,
+// through a mapa address).  Only a change of value matters to the readers,
+// so plain volatile/relaxed accesses suffice: no ordering is implied.
+__device__ __forceinline__ void st_volatile_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.relaxed.cluster.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -106,3 +106,63 @@ def test_k_split_missing_partial_sums_time_out(extra):
     assert pws.gemm_device_status() == pws.GEMM_OK
     res = oracle.check_f16(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_np, b_np), K)
     assert res["ok"], res
+
+
+def _tiled_ternary_f16(seed, stream, rows, K, period=8200):
+    # Seeded values in {-1, 0, 1}, a block `period` columns wide repeated
+    # along K and cut at K (cheap to generate at K = 2^20).  Every partial sum
+    # is then an integer below 2^24, exact in fp32 whatever the summation
+    # order, so the GPU result must equal the oracle's exact sum rounded to
+    # f16 bit for bit.  period is not a multiple of the 64-column K block, so
+    # a K block summed twice or skipped changes the result.
+    base = inputs.ints(seed, stream, (rows, period), -1, 1).astype(np.float16)
+    reps = -(-K // period)
+    return np.ascontiguousarray(np.tile(base, (1, reps))[:, :K])
+
+
+@pytest.mark.parametrize("M,N,K,flags,want", [
+    # one 128 x 128 tile, 16384 K blocks: the K split gives each CTA of the
+    # cluster 8192 blocks, and the owners wait for the peer's partial sums
+    (128, 128, 1 << 20, 0, {"cta_group": 1, "k_split": 2}),
+    # one 256 x 512 wide pair tile, 4096 K blocks: the epilogue's wait for
+    # the first half of the accumulator lasts the whole K loop
+    (256, 512, 1 << 18, pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE,
+     {"cta_group": 2, "bn": 512}),
+], ids=["k_split_owner", "wide_epilogue"])
+def test_long_k_loops_outlast_a_short_wait_limit(M, N, K, flags, want):
+    # The wait limit bounds stalls, not work.  With a 2 ms limit and one ring
+    # slot (S = 1: every K block waits for its copy, then its multiply), these
+    # calls' K loops run several times longer than the limit; every wait for
+    # the loop's result restarts its clock whenever the producer issues a K
+    # block, so the calls complete and match the oracle exactly.
+    limit_ms = 2.0
+    a_np = _tiled_ternary_f16(21, 0, M, K)
+    b_np = _tiled_ternary_f16(21, 1, N, K)
+    a = torch.from_numpy(a_np).cuda()
+    b = torch.from_numpy(b_np).cuda()
+    pws.gemm_set_debug_flags(flags)
+    try:
+        plan = pws.gemm_f16_nt_plan(M, N, K, stages=1)
+        assert {k: plan[k] for k in want} == want, plan
+        out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        pws.gemm_f16_nt(a, b, out, stages=1)              # warm: first-call set-up
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status() == pws.GEMM_OK
+        pws.gemm_set_wait_timeout_ns(int(limit_ms * 1e6))
+        out.fill_(0)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        pws.gemm_f16_nt(a, b, out, stages=1)
+        stop.record()
+        torch.cuda.synchronize()
+        elapsed_ms = start.elapsed_time(stop)
+        status = pws.gemm_device_status()
+    finally:
+        pws.gemm_set_debug_flags(0)
+        pws.gemm_set_wait_timeout_ns(0)
+    assert status == pws.GEMM_OK, (pws.gemm_status_string(status), elapsed_ms)
+    # the loop really did outlast the limit, so the test means something
+    assert elapsed_ms > limit_ms, elapsed_ms
+    ref = oracle.gemm_f16_nt_f64(a_np, b_np)
+    got = out.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.f64_to_f16(ref)), int((got != oracle.f64_to_f16(ref)).sum())
