@@ -404,31 +404,42 @@ def extra_configs(pws, torch, stream):
         wl = inputs.WORKLOADS[name]
         a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(name))
         c = torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev)
-        # the ragged shape is timed on both of its paths: repack + TMA (the
-        # default) and the async-copy producer reading the operands in place
-        variants = [("", 0)]
+        # the ragged shape (rows no tensor map describes) is timed on each of
+        # its paths: read in place by the realigning producer (the default:
+        # nothing allocated), repacked into pooled scratch + TMA
+        # (gemm_set_scratch_pool), repacked into the no-alloc call's fixed
+        # array + TMA, and the 4-byte cp.async producer
+        variants = [("", 0, False, pws.gemm_f16_nt)]
         if name.startswith("f16_nt_ragged"):
-            variants.append(("copy_producer", pws.GEMM_DEBUG_FORCE_COPY_PRODUCER))
-        for suffix, flags in variants:
+            variants += [("pooled_repack", 0, True, pws.gemm_f16_nt),
+                         ("noalloc", 0, False, pws.gemm_f16_nt_noalloc),
+                         ("copy_producer", pws.GEMM_DEBUG_FORCE_COPY_PRODUCER, False, pws.gemm_f16_nt)]
+        for suffix, flags, pool, call in variants:
             pws.gemm_set_debug_flags(flags)
+            pws.gemm_set_scratch_pool(pool)
             try:
                 plan = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), wl.stages[0])
-                label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B", 2: "repack+tma"}[plan["producer"]]
+                label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B", 2: "repack+tma",
+                         3: "realign in place"}[plan["producer"]]
+                if call is pws.gemm_f16_nt_noalloc:
+                    label = "repack into the fixed array+tma" if plan["producer"] == 3 else label
                 res = {"producer": label, "cta_group": plan["cta_group"]}
                 small = wl.flops < 2 ** 34        # launch-bound: time from a CUDA graph
                 for s in wl.stages:
-                    if small and not plan["producer"] == 2:
-                        ms = time_graph(lambda st: pws.gemm_f16_nt(a, b, c, stages=s, stream=st), torch)
+                    if small and plan["producer"] in (0, 3) and call is pws.gemm_f16_nt:
+                        ms = time_graph(lambda st: call(a, b, c, stages=s, stream=st), torch)
                     else:
-                        ms = time_steady(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), torch, stream)
+                        ms = time_steady(lambda: call(a, b, c, stages=s, stream=stream), torch, stream)
                     ps = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), s)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
                                     "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1),
                                     "tile": f"{ps['bm']}x{ps['bn']}"}
-                    res[f"S{s}"]["timing"] = ("CUDA-graph replay" if small and not plan["producer"] == 2
+                    res[f"S{s}"]["timing"] = ("CUDA-graph replay"
+                                              if small and plan["producer"] in (0, 3) and call is pws.gemm_f16_nt
                                               else "0.25 s warm-up, then 0.25 s of back-to-back launches")
             finally:
                 pws.gemm_set_debug_flags(0)
+                pws.gemm_set_scratch_pool(False)
             if name == "f16_nt_8192" and not suffix:
                 pairs = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count // 2
                 res["model"] = sweep_model(res, plan, pairs)

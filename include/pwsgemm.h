@@ -125,23 +125,18 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  *
  * The producer uses the tensor memory accelerator (TMA) when both operands
  * start on 16-byte boundaries and K is a multiple of 8 (row stride a multiple
- * of 16 bytes).  Otherwise the call first copies both operands into rows of
- * ceil(K/64)*64 elements (128-byte aligned rows, which the accelerator reads
- * faster than rows at other multiples of 16 bytes) in scratch memory taken,
- * stream-ordered, from a memory pool the library owns on the current device
- * (about (M+N)*ceil(K/64)*128 bytes, each operand's part rounded up to 256
- * bytes, returned to the pool on `stream` after the GEMM; the pool keeps freed
- * memory for the next call, so repeated calls of one size request no new
- * memory and never synchronize).  If the pool cannot supply it, an
- * asynchronous-copy producer fills the same swizzled ring straight from the
- * operands instead.  Partial tiles are zero-filled on load and clipped on
- * store.
+ * of 16 bytes).  Otherwise eight producer warps per CTA read the operands in
+ * place: each row's K strip is loaded as the aligned 16-byte blocks that hold
+ * it, shifted into place in registers and written into the same swizzled ring
+ * slot TMA would fill; any tile shape can use it, and nothing is allocated
+ * (gemm_set_scratch_pool offers a faster path for large such operands that
+ * allocates).  Partial tiles are zero-filled on load and clipped on store.
  *
  * Output tiles: 256 x 256 on a CTA pair (two SMs sharing one tcgen05 MMA),
  * or 128 x 128 on one CTA.  The pair tile is used when TMA feeds it and it
  * needs fewer waves of CTA groups than the single-CTA tile (or as many, with
  * at least as many pair tiles as half the SMs); the asynchronous-copy
- * producer always uses the single-CTA tile.  With stages <= 4 the pair uses
+ * producer (GEMM_DEBUG_FORCE_COPY_PRODUCER) always uses the single-CTA tile.  With stages <= 4 the pair uses
  * a 256 x 512 tile instead where that adds no padding columns: each ring
  * slot then carries two B boxes, so each operand byte copied into shared
  * memory feeds 4/3 as many flops (5 and 6 slots of that size do not fit in
@@ -289,6 +284,27 @@ enum {
 int gemm_set_debug_flags(unsigned flags);
 
 /*
+ * gemm_set_scratch_pool -- whether later gemm_f16_nt calls may allocate
+ * scratch memory (host state only; default 0 = never).
+ *
+ * Off (the default), operands that the tensor memory accelerator cannot
+ * address (rows not a multiple of 16 bytes apart, or a base not 16-byte
+ * aligned) are read in place by the realigning producer, and no call
+ * allocates device memory.  On, such operands are first copied into rows of
+ * ceil(K/64)*64 elements in scratch memory taken stream-ordered from a
+ * memory pool the library owns on the current device (about
+ * (M+N)*ceil(K/64)*128 bytes per call, returned to the pool on `stream`
+ * after the GEMM; the pool keeps freed memory, so repeated calls of one size
+ * request no new memory from the driver), and the copy is read with TMA.
+ * That copy pays for itself on large operands: measured on GB300 at
+ * 4000 x 3000 x 2050, S = 3, the call takes 49 us with the pool and 140 us
+ * in place.  If the pool cannot supply the scratch, the call reads the
+ * operands in place after all.  Results are bitwise identical either way.
+ * Returns GEMM_OK.
+ */
+int gemm_set_scratch_pool(int enable);
+
+/*
  * gemm_f16_nt_plan -- the launch plan gemm_f16_nt would use for these
  * arguments, without touching a device (host logic only).  Validates the
  * arguments exactly as gemm_f16_nt does and returns the same status.
@@ -296,6 +312,7 @@ int gemm_set_debug_flags(unsigned flags);
  *   plan[2] K per ring slot (BK)              plan[3] CTAs per tile (1 or 2)
  *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy,
  *           2 = tensor memory accelerator on an aligned scratch copy
+ *           (gemm_set_scratch_pool), 3 = realigning loads in place
  *   plan[5] copy granularity in bytes (16 for TMA, else 8, 4 or 2)
  *   plan[6] output store: 0 = tensor memory accelerator, 1 = plain stores
  *   plan[7] dynamic shared memory bytes per CTA

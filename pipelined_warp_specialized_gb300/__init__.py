@@ -78,6 +78,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gemm_set_wait_timeout_ns.restype = i32
     lib.gemm_set_debug_flags.argtypes = [u32]
     lib.gemm_set_debug_flags.restype = i32
+    lib.gemm_set_scratch_pool.argtypes = [i32]
+    lib.gemm_set_scratch_pool.restype = i32
     lib.gemm_f16_nt_plan.argtypes = [i64, i64, i64, vp, vp, vp, i32, ctypes.POINTER(i64)]
     lib.gemm_f16_nt_plan.restype = i32
     if path is None:
@@ -233,6 +235,12 @@ def gemm_set_debug_flags(flags: int) -> None:
     _check(load_library().gemm_set_debug_flags(int(flags)), "gemm_set_debug_flags")
 
 
+def gemm_set_scratch_pool(enable: bool) -> None:
+    """Lets later gemm_f16_nt calls copy operands TMA cannot address to pooled
+    scratch (faster for large ones; allocates stream-ordered).  Off by default."""
+    _check(load_library().gemm_set_scratch_pool(int(bool(enable))), "gemm_set_scratch_pool")
+
+
 def gemm_f16_nt_plan(M: int, N: int, K: int, lhs_ptr: int = 1 << 40, rhs_ptr: int = 2 << 40,
                      out_ptr: int = 3 << 40, stages: int = 4) -> dict:
     """The launch plan gemm_f16_nt would use (host logic only; the pointers are
@@ -246,5 +254,6 @@ def gemm_f16_nt_plan(M: int, N: int, K: int, lhs_ptr: int = 1 << 40, rhs_ptr: in
 
 __all__ = [
     "GemmError", "load_library", "header_functions", "gemm_s32_nn", "gemm_f16_nt", "gemm_device_status",
-    "gemm_status_string", "gemm_set_wait_timeout_ns", "gemm_set_debug_flags", "gemm_f16_nt_plan",
+    "gemm_status_string", "gemm_set_wait_timeout_ns", "gemm_set_debug_flags", "gemm_set_scratch_pool",
+    "gemm_f16_nt_plan", "gemm_f16_nt_noalloc", "gemm_s32_nn_ring",
 ]

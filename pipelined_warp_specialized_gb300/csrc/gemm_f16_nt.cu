@@ -94,8 +94,11 @@ constexpr int EPI_COLS = 64;           // output columns per epilogue chunk (128
 constexpr int EPI_BUF = 32 * EPI_COLS * 2;     // 32 rows x 64 columns
 constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
 static_assert(EPI_WARPS_WIDE * EPI_BUF == EPI_BYTES, "both epilogue forms use the same staging bytes");
-template <int NW>
-constexpr int epi_warps() { return NW == 2 ? EPI_WARPS_WIDE : EPI_WARPS; }
+// The wide tile fed by TMA drains with eight warps (two per lane quarter, a
+// half of the chunks each); fed by the realigning producer it drains with
+// four, leaving the registers of a 13-warp block to the producer's loads.
+template <int NW, int PK>
+constexpr int epi_warps() { return NW == 2 && PK == 0 ? EPI_WARPS_WIDE : EPI_WARPS; }
 constexpr int MAX_STAGES = 6;
 constexpr int COPY_WARPS = 8;          // producer warps of the cp.async producer
 constexpr int COPY_THREADS = COPY_WARPS * 32;
@@ -104,14 +107,16 @@ constexpr int COPY_THREADS = COPY_WARPS * 32;
 #endif
 constexpr int GROUP_M = PWS_GROUP_M;   // tile-row group height of the raster order
 
-enum { kProducerTma = 0, kProducerCopy = 1 };
+// kProducerRealign: aligned 16-byte loads shifted into place, any tile (the
+// plan query reports the repack path as 2)
+enum { kProducerTma = 0, kProducerCopy = 1, kProducerRealign = 3 };
 enum { kStoreTma = 0, kStoreDirect = 1 };
 
 struct Params {
     int M, N, K;
     int num_kb;                 // K blocks: cdiv(K, BK)
     int tiles_m, tiles_n, num_tiles;
-    int producer;               // kProducerTma / kProducerCopy
+    int producer;               // kProducerTma / kProducerCopy / kProducerRealign
     int copy_bytes;             // cp.async granularity (8, 4) or 2 (plain loads)
     int store;                  // kStoreTma / kStoreDirect
     unsigned flags;             // GEMM_DEBUG_* bits
@@ -251,6 +256,13 @@ struct Waiter {
     // hand-over's): the limit counts from the start of the wait.
     template <bool CLUSTER_SCOPE = false>
     __device__ bool wait(uint32_t bar, uint32_t parity) const {
+        return wait_inline<CLUSTER_SCOPE>(bar, parity);
+    }
+
+    // The same, inlined into the caller: for a caller holding many registers
+    // across the wait (the realigning producer's loads in flight).
+    template <bool CLUSTER_SCOPE = false>
+    __device__ __forceinline__ bool wait_inline(uint32_t bar, uint32_t parity) const {
         if (probe<CLUSTER_SCOPE>(bar, parity)) return true;
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
@@ -396,10 +408,205 @@ __device__ void copy_producer(const Params& p, const Waiter& W, uint32_t sA, uin
     }
 }
 
-// A CTA pair is always fed by TMA (one producer warp): its bound lets the
-// compiler use the registers the cp.async producer's eight warps would need.
-template <int CG, int S, int NW>
-__global__ void __launch_bounds__((CG == 2 ? 1 + 1 + epi_warps<NW>() : COPY_WARPS + 1 + EPI_WARPS) * 32, 1)
+// ---------------------------------------------------------------- realigning producer
+//
+// Reads the operands in place where no tensor map can describe them (rows
+// not a multiple of 16 bytes apart, or a base not 16-byte aligned) and writes
+// the slot layout TMA writes, so any tile can use it and nothing is copied
+// to scratch memory.  Partial tiles follow the pages' cdiv and if guards
+// (Croqtile tutorial ch.6 "带 event 的 1P1C 内核", ch.5 "以 if 实现谓词执行"):
+// rows past M or N and columns past K are written as zeros.
+//
+// A warp operation covers 4 rows of a strip, 8 lanes per row, each lane one
+// 16-byte chunk of the row's 64-element K strip.  Its 4 rows are 8 rows
+// apart: strip row i = c + 8 j, with class c = i mod 8.  A strip starts at a
+// multiple of 64 rows and 8 rows span 16 K bytes, so every row of class c
+// starts (base + 2 c K) mod 16 bytes past a 16-byte boundary in every strip
+// and K block.  The 4 rows of an operation therefore share one shift, taken
+// by a warp-uniform switch, and the 128-byte swizzle of their chunks (chunk
+// XOR row mod 8) is the chunk index XOR c.  Each lane loads the aligned
+// 16-byte block holding the start of its chunk and, unless the shift is zero,
+// the next one, and shifts the chunk into place; each block read holds a
+// byte the chunk needs, so no load leaves the operand's pages.
+//
+// A warp issues the loads of a batch of its operations before it waits for
+// the slot (registers, not shared memory, hold them), then writes them; the
+// slot is signalled after a proxy fence (the tensor core reads through the
+// async proxy) with one arrive per warp -- on the leader CTA's full[s], at
+// cluster scope, for a CTA pair.
+
+// Bytes SH .. SH+15 of the 32 bytes lo | hi (little-endian), SH even.
+template <int SH>
+__device__ __forceinline__ uint4 shift_chunk(const uint4& lo, const uint4& hi) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    constexpr int q = SH / 4, r = SH % 4;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = r == 0 ? w[i + q] : __funnelshift_r(w[i + q], w[i + q + 1], 8 * r);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 shift_chunk_any(const uint4& lo, const uint4& hi, int sh) {
+    switch (sh) {
+        case 0: return lo;
+        case 2: return shift_chunk<2>(lo, hi);
+        case 4: return shift_chunk<4>(lo, hi);
+        case 6: return shift_chunk<6>(lo, hi);
+        case 8: return shift_chunk<8>(lo, hi);
+        case 10: return shift_chunk<10>(lo, hi);
+        case 12: return shift_chunk<12>(lo, hi);
+        default: return shift_chunk<14>(lo, hi);
+    }
+}
+
+// One unit's K loop of the realigning producer.  NOPS operations per warp
+// and K block: the 4 of A's strip (operations w, w + 8, w + 16, w + 24 of its
+// 32), then those of the B boxes; SMALL: one 64-row B box (half-width unit of
+// the 256 x 256 / 128 x 128 tiles, 16 operations, class (w >> 1) + 4 i), else
+// 128-row boxes (class (w >> 2) + 2 i, box h = i / 4).  Every per-operation
+// quantity is a compile-time multiple of a per-lane term.  Returns false if
+// a wait gave up.
+template <int CG, int NW, int S, int NOPS, bool SMALL>
+__device__ __forceinline__ bool realign_unit(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB,
+                                             uint32_t full_addr, uint32_t bEMPTY, uint32_t progress, int kb0,
+                                             int kb1, int m_cta, int n_cta, uint32_t shA, uint32_t shB, int warp,
+                                             int lane, uint32_t& stage, uint32_t& phase, uint32_t& issued) {
+    using SH = Shape<CG, NW>;
+    using L = Layout<S, NW>;
+    const int r4 = lane >> 3, cl = lane & 7;
+    const uint64_t rb = 2ull * static_cast<uint32_t>(p.K);          // bytes between rows
+    // A (and 128-row B boxes): class c0 + 2 i, rows 8 j + class
+    const int jA = 4 * (warp & 3) + r4, c0A = warp >> 2;
+    // a 64-row B box: class c0 + 4 i
+    const int jB = SMALL ? 4 * (warp & 1) + r4 : jA, c0B = SMALL ? warp >> 1 : c0A;
+    const int rowA = m_cta + c0A + 8 * jA, rowB = n_cta + c0B + 8 * jB;
+    const uintptr_t pA = reinterpret_cast<uintptr_t>(p.lhs) + static_cast<uintptr_t>(static_cast<uint64_t>(rowA) * rb);
+    const uintptr_t pB = reinterpret_cast<uintptr_t>(p.rhs) + static_cast<uintptr_t>(static_cast<uint64_t>(rowB) * rb);
+    const uint32_t dA = static_cast<uint32_t>(c0A + 8 * jA) * 128u, dB = static_cast<uint32_t>(c0B + 8 * jB) * 128u;
+    const uint32_t xA = static_cast<uint32_t>(cl ^ c0A) << 4, xB = static_cast<uint32_t>(cl ^ c0B) << 4;
+    const uint32_t shA0 = shA >> (4 * c0A), shB0 = shB >> (4 * c0B);
+    for (int kb = kb0; kb < kb1; ++kb) {
+        const int vb = min(2 * (p.K - kb * BK), 2 * BK);             // bytes of each row in this K block
+        const uintptr_t koff = static_cast<uintptr_t>(kb) * (2 * BK);
+        const uint32_t slotA = sA + stage * A_SLOT, slotB = sB + stage * L::B_STRIDE;
+        const bool lo_in = 16 * cl < vb;
+        uint4 lo[NOPS], hi[NOPS];
+        // the loads of the whole K block first: they touch no shared memory,
+        // so they are in flight while the warp waits for the slot
+#pragma unroll
+        for (int i = 0; i < NOPS; ++i) {
+            const bool is_a = i < 4;
+            const int q = is_a ? i : (SMALL ? i - 4 : (i - 4) & 3);
+            const int h = is_a || SMALL ? 0 : (i - 4) >> 2;
+            const int cstep = !is_a && SMALL ? 4 : 2;
+            const int roff = h * SH::UMMA_N + cstep * q;
+            const int sh = static_cast<int>(((is_a ? shA0 : shB0) >> (4 * cstep * q)) & 15u);
+            const bool row_ok = is_a ? rowA + roff < p.M : rowB + roff < p.N;
+            const uintptr_t src = (is_a ? pA : pB) + static_cast<uintptr_t>(static_cast<uint64_t>(roff) * rb) + koff;
+            const uint4* blk = reinterpret_cast<const uint4*>(src - static_cast<uintptr_t>(sh)) + cl;
+            lo[i] = make_uint4(0u, 0u, 0u, 0u);
+            hi[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (row_ok && lo_in) lo[i] = __ldg(blk);
+            if (row_ok && sh != 0 && 16 * (cl + 1) < sh + vb) hi[i] = __ldg(blk + 1);
+        }
+        bool got = true;
+        if (lane == 0) got = W.wait_inline(bEMPTY + 8 * stage, phase);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) return false;
+        const int rem = vb - 16 * cl;                                 // bytes of the chunk inside K
+#pragma unroll
+        for (int i = 0; i < NOPS; ++i) {
+            const bool is_a = i < 4;
+            const int q = is_a ? i : (SMALL ? i - 4 : (i - 4) & 3);
+            const int h = is_a || SMALL ? 0 : (i - 4) >> 2;
+            const int cstep = !is_a && SMALL ? 4 : 2;
+            const int sh = static_cast<int>(((is_a ? shA0 : shB0) >> (4 * cstep * q)) & 15u);
+            // strip row c + 8 j at 128 (c + 8 j); chunk cl at (cl ^ c) -- with
+            // c = c0 + cstep q, cl ^ c = (cl ^ c0) ^ (cstep q)
+            const uint32_t dst = (is_a ? slotA + dA : slotB + h * B_SLOT + dB) + static_cast<uint32_t>(cstep * q) * 128u +
+                                 ((is_a ? xA : xB) ^ (static_cast<uint32_t>(cstep * q) << 4));
+            uint4 o = shift_chunk_any(lo[i], hi[i], sh);
+            if (rem < 16) {
+                // the K tail: elements past K are zero
+                uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = 4 * e + 4 <= rem ? w[e] : (4 * e + 2 == rem ? (w[e] & 0xFFFFu) : 0u);
+                o = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x), "r"(o.y), "r"(o.z),
+                         "r"(o.w)
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if constexpr (CG == 1) mbar_arrive(full_addr + 8 * stage);
+            else mbar_arrive_cluster(full_addr + 8 * stage);
+        }
+        ++issued;
+        if (warp == 0 && lane == 0) st_volatile_shared_u32(progress, issued);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+    return true;
+}
+
+// The unit's K loop for rows whose starts are all 4-byte aligned (K even,
+// both bases 4-byte aligned; the shifts are then 0, 4, 8 or 12 bytes).  A
+// lane loads its chunk where it lies, as one 16-byte, two 8-byte or four
+// 4-byte loads by the class's alignment (a warp-uniform choice), so it needs
+// neither the next block nor a shift, and 4 registers per operation: enough
+// to load K block k + 1 while K block k is written.  Each load holds a byte of
+// its row inside K (the K tail is masked afterwards), so none leaves the
+// operand's pages.
+template <int CG, int NW, int S>
+__device__ void realign_producer(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB, uint32_t bFULL,
+                                 uint32_t bEMPTY, uint32_t progress, int cluster_id, int num_clusters, int kb0,
+                                 int kb1, uint32_t rank, int warp, int lane) {
+    using SH = Shape<CG, NW>;
+    static_assert(COPY_WARPS == 8, "operation mapping: warp w takes operations w, w + 8, ...");
+    const uint32_t full_addr = (CG == 2) ? mapa_shared(bFULL, 0) : bFULL;
+    const uintptr_t a_base = reinterpret_cast<uintptr_t>(p.lhs), b_base = reinterpret_cast<uintptr_t>(p.rhs);
+    const uint64_t rb = 2ull * static_cast<uint32_t>(p.K);
+    // shift of the rows of class c (row mod 8) past a 16-byte boundary, 4 bits per class
+    uint32_t shA = 0u, shB = 0u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        shA |= static_cast<uint32_t>((a_base + static_cast<uintptr_t>(c * rb)) & 15u) << (4 * c);
+        shB |= static_cast<uint32_t>((b_base + static_cast<uintptr_t>(c * rb)) & 15u) << (4 * c);
+    }
+    uint32_t stage = 0, phase = 0, issued = 0;
+    for (int u = cluster_id; u < p.total_units; u += num_clusters) {
+        const Unit un = unit_of(u, p);
+        int tm, tn;
+        tile_coords(un.tile, p, tm, tn);
+        const bool halfw = un.half >= 0;
+        const int m_cta = tm * SH::UMMA_M + static_cast<int>(rank) * BM_CTA;
+        const int n_unit = tn * SH::TILE_N + (halfw ? un.half * SH::HALF_N : 0);
+        bool ok;
+        if (NW == 1 && halfw) {
+            const int n_cta = n_unit + static_cast<int>(rank) * (BN_CTA / 2);
+            ok = realign_unit<CG, NW, S, 6, true>(p, W, sA, sB, full_addr, bEMPTY, progress, kb0, kb1, m_cta, n_cta,
+                                                  shA, shB, warp, lane, stage, phase, issued);
+        } else if (NW == 2 && !halfw) {
+            const int n_cta = n_unit + static_cast<int>(rank) * BN_CTA;
+            ok = realign_unit<CG, NW, S, 12, false>(p, W, sA, sB, full_addr, bEMPTY, progress, kb0, kb1, m_cta,
+                                                    n_cta, shA, shB, warp, lane, stage, phase, issued);
+        } else {
+            const int n_cta = n_unit + static_cast<int>(rank) * BN_CTA;
+            ok = realign_unit<CG, NW, S, 8, false>(p, W, sA, sB, full_addr, bEMPTY, progress, kb0, kb1, m_cta, n_cta,
+                                                   shA, shB, warp, lane, stage, phase, issued);
+        }
+        if (!ok) return;
+    }
+}
+
+// PK = 1: launched with COPY_WARPS producer warps (the cp.async or the
+// realigning producer), PK = 0: with one (TMA).  Single-CTA kernels serve
+// every producer with one bound; a CTA pair has a kernel per producer kind,
+// so the TMA one keeps the registers eight producer warps would take.
+template <int CG, int S, int NW, int PK>
+__global__ void __launch_bounds__(((CG == 1 || PK == 1 ? COPY_WARPS : 1) + 1 + epi_warps<NW, PK>()) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ Params p) {
@@ -414,7 +621,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    constexpr int EW = epi_warps<NW>();
+    constexpr int EW = epi_warps<NW, PK>();
     const int P = static_cast<int>(blockDim.x / 32) - 1 - EW;          // producer warps
     const int mma_warp = P;
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
@@ -438,8 +645,9 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
-        // TMA: one arrive.expect_tx per phase; cp.async: one arrive per producer warp
-        const uint32_t full_count = p.producer == kProducerTma ? 1u : static_cast<uint32_t>(P);
+        // TMA: one arrive.expect_tx per phase; otherwise one arrive per
+        // producer warp (of both CTAs of a pair)
+        const uint32_t full_count = p.producer == kProducerTma ? 1u : static_cast<uint32_t>(P * CG);
         for (int s = 0; s < S; ++s) {
             mbar_init(bFULL + 8 * s, full_count);
             mbar_init(bEMPTY + 8 * s, 1);
@@ -547,6 +755,12 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
                 }
             }
+        } else if (p.producer == kProducerRealign) {
+            if constexpr (CG == 1 || PK == 1) {
+                const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
+                realign_producer<CG, NW, S>(p, W, sA, sB, bFULL, bEMPTY, sPROGRESS, cluster_id, num_clusters, kb0,
+                                            kb1, rank, warp, lane);
+            }
         } else if constexpr (CG == 1) {
             // cp.async producer (single CTA only): COPY_WARPS warps fill the swizzled slot
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
@@ -567,6 +781,9 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         if (is_leader && lane == 0) {
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleMma};
+            // a pair's realigning producer warps arrive on full[s] from both
+            // CTAs with release at cluster scope: acquire at cluster scope
+            constexpr bool kFullCluster = CG == 2 && PK == 1;
             uint32_t stage = 0, phase = 0;
             bool ok = true, issued_any = false;
             if constexpr (NW == 1) {
@@ -599,7 +816,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                             ph[1] = stage + 1 == S ? phase ^ 1u : phase;
                         }
                         for (int j = 0; j < nb; ++j)
-                            if (!W.wait(bFULL + 8 * st[j], ph[j])) { ok = false; break; }
+                            if (!W.template wait<kFullCluster>(bFULL + 8 * st[j], ph[j])) { ok = false; break; }
                         if (!ok) break;
                         tc_fence_after_sync();
                         if (p.producer == kProducerCopy) fence_proxy_async_smem();
@@ -660,7 +877,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         tc_mma_f16<CG>(d, a + 2 * k, b + 2 * k, IDESC, !(first && k == 0));
                 };
                 auto wait_full = [&]() {
-                    if (!W.wait(bFULL + 8 * stage, phase)) return false;
+                    if (!W.template wait<kFullCluster>(bFULL + 8 * stage, phase)) return false;
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                     return true;
                 };
@@ -879,9 +1096,10 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             const int nch = ncols / EPI_COLS;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col0;
             // the wide tile's two warps of a lane quarter take half of the chunks each
-            const int cb = NW == 2 ? (e / 4) * (nch / 2) : 0;
-            const int ce = NW == 2 ? cb + nch / 2 : nch;
-            if (NW == 2 && p.store == kStoreTma) {
+            constexpr bool kHalfChunks = EW == EPI_WARPS_WIDE;
+            const int cb = kHalfChunks ? (e / 4) * (nch / 2) : 0;
+            const int ce = kHalfChunks ? cb + nch / 2 : nch;
+            if (kHalfChunks && p.store == kStoreTma) {
                 // one staging buffer per warp
                 const uint32_t buf = sEPI + static_cast<uint32_t>(e) * EPI_BUF;
                 for (int c = cb; c < ce; ++c) {
@@ -896,6 +1114,27 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const int col0 = col_base + c * EPI_COLS;
                     if (lane == 0 && row0 < p.M && col0 < p.N) {
                         tma_store_2d(&tmC, buf, col0, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (NW == 2 && p.store == kStoreTma) {
+                // four warps: each drains all chunks of its lane quarter, one
+                // at a time through its two staging buffers in turn (a bulk
+                // group per chunk, possibly empty, so that "at most one group
+                // still reading" means the buffer about to be written is free)
+                const uint32_t bufs = sEPI + static_cast<uint32_t>(e) * 2 * EPI_BUF;
+                for (int c = 0; c < nch; ++c) {
+                    const uint32_t buf = bufs + static_cast<uint32_t>(c & 1) * EPI_BUF;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    uint32_t h[32];
+                    load_chunk(tbase, c, h);
+                    stage_chunk(buf, h);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    const int col0 = col_base + c * EPI_COLS;
+                    if (lane == 0) {
+                        if (row0 < p.M && col0 < p.N) tma_store_2d(&tmC, buf, col0, row0);
                         bulk_commit_group();
                     }
                 }
@@ -1226,9 +1465,11 @@ bool narrow_fills_better(int64_t M, int64_t N, int stages, int64_t pair_cap) {
     return stages >= 3 && wide < pair_cap && 2 * (narrow - pair_cap) <= pair_cap;
 }
 
-// `allow_repack` = false plans the path that needs no scratch memory.
+// Operands that no tensor map can describe are read in place by the
+// realigning producer, unless `repack` is set: then they are copied to
+// aligned rows in scratch memory first and read by TMA.
 Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs, const void* out, int stages,
-               int num_sms, unsigned flags, bool allow_repack = true) {
+               int num_sms, unsigned flags, bool repack = false) {
     Plan pl;
     const uintptr_t a = reinterpret_cast<uintptr_t>(lhs), b = reinterpret_cast<uintptr_t>(rhs);
     const uintptr_t o = reinterpret_cast<uintptr_t>(out);
@@ -1237,9 +1478,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     if (!force_copy && native_tma) {
         pl.producer = kProducerTma;
         pl.copy_bytes = 16;
-    } else if (!force_copy && allow_repack) {
+    } else if (!force_copy && repack) {
         pl.repack = true;
         pl.producer = kProducerTma;
+        pl.copy_bytes = 16;
+    } else if (!force_copy) {
+        pl.producer = kProducerRealign;
         pl.copy_bytes = 16;
     } else {
         pl.producer = kProducerCopy;
@@ -1264,7 +1508,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     const int64_t pair_waves = (pair_tiles + pair_cap - 1) / pair_cap;
     const bool want_pair = (flags & GEMM_DEBUG_FORCE_PAIR_TILE) || pair_waves < solo_waves ||
                            (pair_waves == solo_waves && 2 * pair_tiles >= num_sms);
-    pl.cg = (pl.producer == kProducerTma && !(flags & GEMM_DEBUG_FORCE_SOLO_TILE) && want_pair) ? 2 : 1;
+    pl.cg = (pl.producer != kProducerCopy && !(flags & GEMM_DEBUG_FORCE_SOLO_TILE) && want_pair) ? 2 : 1;
     pl.nw = (pl.cg == 2 && stages <= WIDE_MAX_STAGES && !(flags & GEMM_DEBUG_FORCE_NARROW_TILE) &&
              ((flags & GEMM_DEBUG_FORCE_WIDE_TILE) ||
               (want_wide(N) && !narrow_fills_better(M, N, stages, pair_cap))))
@@ -1294,15 +1538,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
 }
 
 inline int block_threads(const Plan& pl) {
-    return ((pl.producer == kProducerTma ? 1 : COPY_WARPS) + 1 + (pl.nw == 2 ? EPI_WARPS_WIDE : EPI_WARPS)) * 32;
+    const bool tma = pl.producer == kProducerTma;
+    return ((tma ? 1 : COPY_WARPS) + 1 + (pl.nw == 2 && tma ? EPI_WARPS_WIDE : EPI_WARPS)) * 32;
 }
 
 // Sets the kernel's shared-memory limit (once per device) and returns how
 // many CTA groups (pairs or single CTAs) can be resident at once: the size of
 // the persistent grid.  0 on failure.
-template <int CG, int S, int NW>
+template <int CG, int S, int NW, int PK>
 int capacity(const DeviceInfo& info, int threads) {
-    auto kern = gemm_f16_nt_kernel<CG, S, NW>;
+    auto kern = gemm_f16_nt_kernel<CG, S, NW, PK>;
     constexpr int smem = Layout<S, NW>::DYN;
     static_assert(Layout<S, NW>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
     // per-device caches; concurrent first calls from several host threads
@@ -1339,32 +1584,39 @@ int capacity(const DeviceInfo& info, int threads) {
     }
 }
 
-template <int CG, int NW>
+template <int CG, int NW, int PK>
 int capacity_for(int stages, const DeviceInfo& info, int threads) {
     switch (stages) {
-        case 1: return capacity<CG, 1, NW>(info, threads);
-        case 2: return capacity<CG, 2, NW>(info, threads);
-        case 3: return capacity<CG, 3, NW>(info, threads);
-        case 4: return capacity<CG, 4, NW>(info, threads);
+        case 1: return capacity<CG, 1, NW, PK>(info, threads);
+        case 2: return capacity<CG, 2, NW, PK>(info, threads);
+        case 3: return capacity<CG, 3, NW, PK>(info, threads);
+        case 4: return capacity<CG, 4, NW, PK>(info, threads);
     }
-    if constexpr (NW == 1) return stages == 5 ? capacity<CG, 5, 1>(info, threads) : capacity<CG, 6, 1>(info, threads);
+    if constexpr (NW == 1)
+        return stages == 5 ? capacity<CG, 5, 1, PK>(info, threads) : capacity<CG, 6, 1, PK>(info, threads);
     return 0;
 }
 
+// PK of a plan's kernel: single-CTA kernels serve every producer (PK = 0);
+// a CTA pair fed by the realigning producer has its own (PK = 1).
+inline int pk_of(const Plan& pl) { return pl.cg == 2 && pl.producer != kProducerTma ? 1 : 0; }
+
 int capacity_of(const Plan& pl, int stages, const DeviceInfo& info) {
     const int threads = block_threads(pl);
-    if (pl.cg == 1) return capacity_for<1, 1>(stages, info, threads);
-    return pl.nw == 2 ? capacity_for<2, 2>(stages, info, threads) : capacity_for<2, 1>(stages, info, threads);
+    if (pl.cg == 1) return capacity_for<1, 1, 0>(stages, info, threads);
+    if (pk_of(pl))
+        return pl.nw == 2 ? capacity_for<2, 2, 1>(stages, info, threads) : capacity_for<2, 1, 1>(stages, info, threads);
+    return pl.nw == 2 ? capacity_for<2, 2, 0>(stages, info, threads) : capacity_for<2, 1, 0>(stages, info, threads);
 }
 
 // Launches the persistent grid: one CTA group per work unit, at most as many
 // as can be resident.
-template <int CG, int S, int NW>
+template <int CG, int S, int NW, int PK>
 int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
            const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
-    auto kern = gemm_f16_nt_kernel<CG, S, NW>;
+    auto kern = gemm_f16_nt_kernel<CG, S, NW, PK>;
     const int threads = block_threads(pl);
-    const int cap = capacity<CG, S, NW>(info, threads);
+    const int cap = capacity<CG, S, NW, PK>(info, threads);
     if (cap <= 0) return GEMM_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
@@ -1390,27 +1642,30 @@ int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const 
     return GEMM_OK;
 }
 
-template <int CG, int NW>
+template <int CG, int NW, int PK>
 int launch_stages(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
                   const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
     switch (stages) {
-        case 1: return launch<CG, 1, NW>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 2: return launch<CG, 2, NW>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 3: return launch<CG, 3, NW>(pl, info, ta, tb, tbh, tc, p, stream);
-        case 4: return launch<CG, 4, NW>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 1: return launch<CG, 1, NW, PK>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 2: return launch<CG, 2, NW, PK>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 3: return launch<CG, 3, NW, PK>(pl, info, ta, tb, tbh, tc, p, stream);
+        case 4: return launch<CG, 4, NW, PK>(pl, info, ta, tb, tbh, tc, p, stream);
     }
     if constexpr (NW == 1) {
-        if (stages == 5) return launch<CG, 5, 1>(pl, info, ta, tb, tbh, tc, p, stream);
-        if (stages == 6) return launch<CG, 6, 1>(pl, info, ta, tb, tbh, tc, p, stream);
+        if (stages == 5) return launch<CG, 5, 1, PK>(pl, info, ta, tb, tbh, tc, p, stream);
+        if (stages == 6) return launch<CG, 6, 1, PK>(pl, info, ta, tb, tbh, tc, p, stream);
     }
     return GEMM_ERR_UNSUPPORTED_STAGES;
 }
 
 int launch_plan(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
                 const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
-    if (pl.cg == 1) return launch_stages<1, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
-    return pl.nw == 2 ? launch_stages<2, 2>(stages, pl, info, ta, tb, tbh, tc, p, stream)
-                      : launch_stages<2, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    if (pl.cg == 1) return launch_stages<1, 1, 0>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    if (pk_of(pl))
+        return pl.nw == 2 ? launch_stages<2, 2, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream)
+                          : launch_stages<2, 1, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream);
+    return pl.nw == 2 ? launch_stages<2, 2, 0>(stages, pl, info, ta, tb, tbh, tc, p, stream)
+                      : launch_stages<2, 1, 0>(stages, pl, info, ta, tb, tbh, tc, p, stream);
 }
 
 }  // namespace f16nt
@@ -1422,12 +1677,14 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
     const int rc = validate(M, N, K, lhs, rhs, out, stages);
     if (rc != GEMM_OK) return rc;
     if (!plan) return GEMM_ERR_INVALID_ARG;
-    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, pws::sm_count_or_default(), pws::debug_flags());
+    const unsigned flags = pws::debug_flags();
+    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, pws::sm_count_or_default(), flags,
+                              pws::scratch_pool_enabled());
     plan[0] = 128 * pl.cg;
     plan[1] = 128 * pl.cg * pl.nw;
     plan[2] = BK;
     plan[3] = pl.cg;
-    plan[4] = pl.repack ? 2 : pl.producer;
+    plan[4] = pl.repack ? 2 : pl.producer;       // 0 TMA, 1 cp.async, 2 repack + TMA, 3 realigning loads
     plan[5] = pl.copy_bytes;
     plan[6] = pl.store;
     plan[7] = pl.smem;
@@ -1496,18 +1753,20 @@ int run_plan(const Plan& pl, const DeviceInfo& info, int64_t M, int64_t N, int64
     // Tail split: when the tiles leave a last, partial wave of the persistent
     // grid (or fewer tiles than the grid) and twice that many units still
     // fit in one wave, each of those tiles runs as two half-width units on the
-    // wave's otherwise idle CTA groups.  Only the TMA producer supports it
-    // (the 256 x 256 and 128 x 128 tiles need a 64-row B box; a half of the
-    // wide tile is one ordinary box).  Each output element is still one
+    // wave's otherwise idle CTA groups.  The TMA and the realigning producers
+    // support it (with TMA the 256 x 256 and 128 x 128 tiles need a 64-row B
+    // box; a half of the wide tile is one ordinary box).  Each output element is still one
     // in-order K sum; the decision depends on the shape and the device, never
     // on S.
     const int cap = capacity_of(pl, stages, info);
     if (cap <= 0) return GEMM_ERR_LAUNCH;
     const int waves = pl.num_tiles / cap;
     const int tail = pl.num_tiles - waves * cap;
-    if (pl.producer == kProducerTma && pl.ksplit == 1 && tail > 0 && 2 * tail <= cap &&
+    if (pl.producer != kProducerCopy && pl.ksplit == 1 && tail > 0 && 2 * tail <= cap &&
         !(flags & GEMM_DEBUG_NO_SPLIT)) {
-        if (pl.nw == 1 && !encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2)) return GEMM_ERR_LAUNCH;
+        if (pl.producer == kProducerTma && pl.nw == 1 &&
+            !encode_tmap_f16_2d(&tbh, b_src, K, N, ld * 2, BK, BN_CTA / 2))
+            return GEMM_ERR_LAUNCH;
         p.full_units = waves * cap;
         p.split = 2;
         p.total_units = waves * cap + 2 * tail;
@@ -1530,11 +1789,12 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     if (rc != GEMM_OK) return rc;
     if (K == 0) return zero_output(out, M, N, info, stream);
     const unsigned flags = debug_flags();
-    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, scratch_pool_enabled());
 
-    // Operands whose rows TMA cannot address are first copied to 16-byte
-    // aligned rows in pooled scratch memory; without scratch, the cp.async
-    // producer reads them where they are.
+    // Operands whose rows TMA cannot address are read in place by the
+    // realigning producer.  With gemm_set_scratch_pool(1) they are copied to
+    // aligned rows in pooled scratch memory first and read by TMA (if the
+    // pool cannot supply it, they are read in place after all).
     const void* a_src = lhs;
     const void* b_src = rhs;
     int64_t ld = K;
@@ -1555,7 +1815,7 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
             b_src = db;
             ld = Kp;
         } else {
-            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, false);
+            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
         }
     }
     rc = run_plan(pl, info, M, N, K, lhs, rhs, out, a_src, b_src, ld, stages, flags, stream);
@@ -1621,7 +1881,7 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     if (rc != GEMM_OK) return rc;
     if (K == 0) return zero_output(out, M, N, info, stream);
     const unsigned flags = debug_flags();
-    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, true);
 
     const void* a_src = lhs;
     const void* b_src = rhs;
@@ -1631,7 +1891,7 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
         if (repack_bytes(M, N, K, &b_off, 8) > kNoAllocScratchBytes) {
             // more scratch than the array holds: the producer that reads the
             // operands in place needs none
-            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, false);
+            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
         } else {
             void* scratch = noalloc_scratch(info.device);
             if (!scratch) return GEMM_ERR_LAUNCH;

@@ -31,6 +31,8 @@ int current_device(DeviceInfo* info);
 
 uint64_t wait_timeout_ns();
 unsigned debug_flags();
+// gemm_set_scratch_pool: gemm_f16_nt may copy unaligned operands to pooled scratch
+bool scratch_pool_enabled();
 
 // SM count of the current device if one is present, else the GB300 count.
 int sm_count_or_default();

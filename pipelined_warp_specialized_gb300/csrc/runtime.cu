@@ -22,6 +22,7 @@ bool g_info_ready[kMaxDevices] = {};
 
 std::atomic<uint64_t> g_timeout_ns{0};
 std::atomic<unsigned> g_flags{0};
+std::atomic<int> g_scratch_pool{0};
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -83,6 +84,8 @@ uint64_t wait_timeout_ns() {
 }
 
 unsigned debug_flags() { return g_flags.load(std::memory_order_relaxed); }
+
+bool scratch_pool_enabled() { return g_scratch_pool.load(std::memory_order_relaxed) != 0; }
 
 int sm_count_or_default() {
     int dev = -1, n = 0;
@@ -181,6 +184,11 @@ const char* gemm_status_string(int status) {
 
 int gemm_set_wait_timeout_ns(uint64_t ns) {
     pws::g_timeout_ns.store(ns, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+int gemm_set_scratch_pool(int enable) {
+    pws::g_scratch_pool.store(enable ? 1 : 0, std::memory_order_relaxed);
     return GEMM_OK;
 }
 

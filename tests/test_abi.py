@@ -251,13 +251,22 @@ def test_plan_k_split_rule(lib):
 
 def test_plan_ragged_shape(lib):
     # K = 2050: rows of 4100 bytes are not 16-byte aligned, so no TMA descriptor
-    # exists for the operands as given: they are repacked, then fed by TMA
+    # exists for the operands as given: the realigning producer reads them in
+    # place (nothing is allocated), on the same tile TMA would get
     p = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
-    assert p["producer"] == 2 and p["copy_bytes"] == 16
+    assert p["producer"] == 3 and p["copy_bytes"] == 16
     assert p["cta_group"] == 2 and p["bm"] == 256               # 16 x 12 pair tiles >= 152 / 2
     assert p["bn"] == 512                       # N = 3000: 6 wide tile columns pad no more than 12 narrow ones
     assert p["store"] == 0                      # 6000-byte output rows are 16-byte aligned
     assert p["tiles"] == 16 * 6 and p["k_blocks"] == 33
+    # with the scratch pool allowed they are repacked, then fed by TMA: same tile
+    pws.gemm_set_scratch_pool(True)
+    try:
+        r = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
+    finally:
+        pws.gemm_set_scratch_pool(False)
+    assert r["producer"] == 2 and {k: r[k] for k in ("bm", "bn", "tiles")} == {k: p[k] for k in ("bm", "bn", "tiles")}
+    assert pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)["producer"] == 3      # the setter is host state
     # the async-copy producer reads them in place (single-CTA tile, 4-byte copies)
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
     try:
@@ -284,9 +293,9 @@ def test_plan_rejects_tile_counts_beyond_int(lib):
 
 
 def test_plan_edge_cases(lib):
-    assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 2            # odd K: repacked
+    assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 3            # odd K: read in place
     assert pws.gemm_f16_nt_plan(7, 9, 3)["store"] == 1               # odd N: plain stores
-    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 2   # unaligned base
+    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 3   # unaligned base
     assert pws.gemm_f16_nt_plan(64, 64, 16)["producer"] == 0
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
     try:
@@ -302,7 +311,7 @@ def test_plan_edge_cases(lib):
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE)
     try:
         assert pws.gemm_f16_nt_plan(300, 300, 64)["cta_group"] == 2
-        assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 2   # repacked, then TMA
+        assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 2   # read in place on the pair tile
     finally:
         pws.gemm_set_debug_flags(0)
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)

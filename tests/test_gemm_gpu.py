@@ -33,14 +33,20 @@ def _dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
+# `flags` value standing for gemm_set_scratch_pool(1) in the parametrized tests
+POOL = 1 << 30
+
+
 def run_f16(a, b, stages, flags=0):
-    pws.gemm_set_debug_flags(flags)
+    pws.gemm_set_debug_flags(flags & ~POOL)
+    pws.gemm_set_scratch_pool(bool(flags & POOL))
     try:
         out = pws.gemm_f16_nt(_dev(a), _dev(b), stages=stages)
         torch.cuda.synchronize()
         assert pws.gemm_device_status() == pws.GEMM_OK
     finally:
         pws.gemm_set_debug_flags(0)
+        pws.gemm_set_scratch_pool(False)
     return out.cpu().numpy()
 
 
@@ -364,40 +370,105 @@ def test_f16_k_zero_and_empty():
     assert out.shape == (0, 4)
 
 
-@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER], ids=["repack", "copy"])
+@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE,
+                                   pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE,
+                                   pws.GEMM_DEBUG_FORCE_KSPLIT, POOL,
+                                   pws.GEMM_DEBUG_FORCE_COPY_PRODUCER],
+                         ids=["realign", "realign_pair", "realign_wide", "realign_ksplit", "repack", "copy"])
 def test_f16_unaligned_operands(flags):
     M, N, K = 150, 90, 128
     big_a = _dev(inputs.uniform_f16(5, 0, (M * K + 1,)))
     a_t = big_a[1:].view(M, K)                           # 2-byte aligned only
     b = inputs.uniform_f16(5, 1, (N, K))
-    pws.gemm_set_debug_flags(flags)
+    pws.gemm_set_debug_flags(flags & ~POOL)
+    pws.gemm_set_scratch_pool(bool(flags & POOL))
     try:
         out = pws.gemm_f16_nt(a_t, _dev(b), stages=2)
         torch.cuda.synchronize()
     finally:
         pws.gemm_set_debug_flags(0)
+        pws.gemm_set_scratch_pool(False)
     assert pws.gemm_device_status() == pws.GEMM_OK
     assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b), K)
 
 
 @pytest.mark.parametrize("offset", range(8))
-def test_f16_repack_every_row_alignment(offset):
-    # The repack reads each row as the aligned 16-byte blocks that hold it and
-    # shifts them into place.  lhs starts `offset` elements into a buffer and
-    # rhs 7 - offset; with K odd, consecutive rows start 2 bytes further on,
-    # so every even byte offset 0..14 occurs as a row start, for both
-    # operands, and the last rows end near the buffers' ends.
+def test_f16_unaligned_every_row_alignment(offset):
+    # The realigning producer and the repack both read each row as the aligned
+    # 16-byte blocks that hold it and shift them into place.  lhs starts
+    # `offset` elements into a buffer and rhs 7 - offset; with K odd,
+    # consecutive rows start 2 bytes further on, so every even byte offset
+    # 0..14 occurs as a row start, for both operands, and the last rows end
+    # near the buffers' ends.  In place on the single-CTA, pair and wide
+    # tiles; repacked into pooled scratch and into the no-alloc array.
     M, N, K = 37, 45, 1027
     big_a = _dev(inputs.normal_f16(60 + offset, 0, (M * K + 8,)))
     big_b = _dev(inputs.normal_f16(60 + offset, 1, (N * K + 8,)))
     a_t = big_a[offset:offset + M * K].view(M, K)
     b_t = big_b[7 - offset:7 - offset + N * K].view(N, K)
-    assert pws.gemm_f16_nt_plan(M, N, K, a_t.data_ptr(), b_t.data_ptr(), 3 << 40)["producer"] == 2
-    for fn in (pws.gemm_f16_nt, pws.gemm_f16_nt_noalloc):
-        out = fn(a_t, b_t, stages=2)
-        torch.cuda.synchronize()
+    assert pws.gemm_f16_nt_plan(M, N, K, a_t.data_ptr(), b_t.data_ptr(), 3 << 40)["producer"] == 3
+    ref = oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b_t.cpu().numpy())
+    outs = []
+    for fn, flags in ((pws.gemm_f16_nt, 0), (pws.gemm_f16_nt, pws.GEMM_DEBUG_FORCE_PAIR_TILE),
+                      (pws.gemm_f16_nt, pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE),
+                      (pws.gemm_f16_nt, POOL), (pws.gemm_f16_nt_noalloc, 0)):
+        pws.gemm_set_debug_flags(flags & ~POOL)
+        pws.gemm_set_scratch_pool(bool(flags & POOL))
+        try:
+            out = fn(a_t, b_t, stages=2)
+            torch.cuda.synchronize()
+        finally:
+            pws.gemm_set_debug_flags(0)
+            pws.gemm_set_scratch_pool(False)
         assert pws.gemm_device_status() == pws.GEMM_OK
-        assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b_t.cpu().numpy()), K)
+        assert_f16_ok(out.cpu().numpy(), ref, K)
+        outs.append(out.cpu().numpy().view(np.uint16))
+    # every tile sums each element over K in the same order: the same bits
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("M,N,K,S,flags,want", [
+    (300, 260, 1024, 2, 0, {"cta_group": 1, "k_split": 1}),                       # 9 single-CTA tiles
+    (300, 260, 4096, 2, 0, {"cta_group": 1, "k_split": 2}),                       # K split
+    (1000, 1000, 512, 3, pws.GEMM_DEBUG_FORCE_SOLO_TILE, {"cta_group": 1}),       # tail split, half-width units
+    (2048, 2048, 1024, 2, 0, {"cta_group": 2, "bn": 256}),                        # pair tile, one wave
+    (2600, 2500, 640, 1, pws.GEMM_DEBUG_FORCE_NARROW_TILE, {"cta_group": 2, "bn": 256}),   # 110 tiles: tail split
+    (4000, 3000, 512, 3, 0, {"cta_group": 2, "bn": 512}),                         # wide tile, tail split
+    (4000, 3000, 512, 4, pws.GEMM_DEBUG_NO_SPLIT, {"cta_group": 2, "bn": 512}),
+    (8192, 2048, 256, 6, 0, {"cta_group": 2, "bn": 256}),                         # six slots (paired MMA waits)
+])
+def test_f16_realign_equals_tma_bitwise(M, N, K, S, flags, want):
+    # With K a multiple of 8, operands that start 2 bytes past a 16-byte
+    # boundary are read by the realigning producer; an aligned copy is read
+    # by TMA.  Same tile, same split, same summation order: the same bits.
+    a_np = inputs.uniform_f16(80, 0, (M, K))
+    b_np = inputs.uniform_f16(80, 1, (N, K))
+    big_a = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
+    big_b = torch.empty(N * K + 8, dtype=torch.float16, device="cuda")
+    a_u = big_a[1:1 + M * K].view(M, K)
+    b_u = big_b[3:3 + N * K].view(N, K)
+    a_u.copy_(torch.from_numpy(a_np))
+    b_u.copy_(torch.from_numpy(b_np))
+    a_al, b_al = _dev(a_np), _dev(b_np)
+    pws.gemm_set_debug_flags(flags)
+    try:
+        p_u = pws.gemm_f16_nt_plan(M, N, K, a_u.data_ptr(), b_u.data_ptr(), 3 << 40, S)
+        p_al = pws.gemm_f16_nt_plan(M, N, K, a_al.data_ptr(), b_al.data_ptr(), 3 << 40, S)
+        assert p_u["producer"] == 3 and p_al["producer"] == 0
+        assert {k: p_u[k] for k in want} == want, p_u
+        assert all(p_u[k] == p_al[k] for k in ("bm", "bn", "cta_group", "k_split", "tiles")), (p_u, p_al)
+        got = pws.gemm_f16_nt(a_u, b_u, stages=S)
+        want_out = pws.gemm_f16_nt(a_al, b_al, stages=S)
+        torch.cuda.synchronize()
+    finally:
+        pws.gemm_set_debug_flags(0)
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    assert np.array_equal(got.cpu().numpy().view(np.uint16), want_out.cpu().numpy().view(np.uint16))
+    rows, cols = _sampled_entries(M, N, 81, 4000)
+    ref = oracle.gemm_f16_nt_entries(a_np, b_np, rows, cols)
+    res = oracle.check_f16(got.cpu().numpy()[rows, cols], ref, K)
+    assert res["ok"], res
 
 
 @pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER,
@@ -455,19 +526,30 @@ def test_f16_4096_config_full():
 
 
 def test_f16_ragged_config_full():
-    # K = 2050: the default path repacks the operands and runs the TMA pair
-    # tile; the async-copy producer reads them in place.  Both against the oracle.
+    # K = 2050: rows of 4100 bytes, which no tensor map describes.  The
+    # default path reads them in place with the realigning producer on the
+    # wide pair tile; also on the 256 x 256 pair and the single-CTA tiles, the
+    # pooled repack + TMA and the async-copy producer.  All against the
+    # oracle, and the tiles bitwise equal to each other.
     wl = inputs.WORKLOADS["f16_nt_ragged_4000x3000x2050"]
     a, b = wl.lhs(), wl.rhs()
-    assert pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K)["producer"] == 2
+    p = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, stages=3)
+    assert (p["producer"], p["cta_group"], p["bn"]) == (3, 2, 512)
     ref = oracle.gemm_f16_nt_f64(a, b)
-    assert_f16_ok(run_f16(a, b, 3), ref, wl.K)
-    assert_f16_ok(run_f16(a, b, 3, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER), ref, wl.K)
+    outs = []
+    for flags in (0, pws.GEMM_DEBUG_FORCE_NARROW_TILE, pws.GEMM_DEBUG_FORCE_SOLO_TILE,
+                  POOL, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER):
+        got = run_f16(a, b, 3, flags)
+        assert_f16_ok(got, ref, wl.K)
+        outs.append(got.view(np.uint16))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
 
 
 def test_f16_repack_scratch_is_stream_ordered():
     # two unaligned-K GEMMs in flight on two streams, each with its own pooled
-    # scratch, repeated so the pool hands blocks back and out again
+    # scratch (gemm_set_scratch_pool), repeated so the pool hands blocks
+    # back and out again
     M, N, K = 640, 520, 1030
     cases = []
     for seed in (41, 42):
@@ -477,8 +559,13 @@ def test_f16_repack_scratch_is_stream_ordered():
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     outs = [torch.empty(M, N, dtype=torch.float16, device="cuda") for _ in range(2)]
     for _ in range(3):
-        for (a, b, da, db, _), s, o in zip(cases, streams, outs):
-            pws.gemm_f16_nt(da, db, o, stages=4, stream=s)
+        pws.gemm_set_scratch_pool(True)
+        try:
+            assert pws.gemm_f16_nt_plan(M, N, K)["producer"] == 2
+            for (a, b, da, db, _), s, o in zip(cases, streams, outs):
+                pws.gemm_f16_nt(da, db, o, stages=4, stream=s)
+        finally:
+            pws.gemm_set_scratch_pool(False)
         torch.cuda.synchronize()
         assert pws.gemm_device_status() == pws.GEMM_OK
         for (a, b, da, db, ref), o in zip(cases, outs):
