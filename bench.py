@@ -364,23 +364,64 @@ def concurrency_configs(pws, torch, G=16, stream_counts=(1, 2, 4, 8)):
     return out
 
 
-def sweep_model(res, plan, pairs):
+def sweep_model(res, plan, pairs, hi=4):
     """The pipeline cost model (TileLang tutorial ch.22, section 1.1) fitted
-    to the sweep's S = 1 and S = 4 points (the same wide tile), and its
-    prediction for S = 2 and 3 beside the measurement."""
+    to the sweep's S = 1 and S = hi points (one tile throughout), and its
+    prediction for S = 2 .. hi-1 beside the measurement."""
     from pipelined_warp_specialized_gb300 import cost_model
-    if not all(f"S{s}" in res and res[f"S{s}"]["tile"] == res["S1"]["tile"] for s in (1, 2, 3, 4)):
+    mids = tuple(range(2, hi))
+    if not all(f"S{s}" in res and res[f"S{s}"]["tile"] == res["S1"]["tile"] for s in (1, hi) + mids):
         return None
-    units = plan["tiles"]                       # wide tiles, one wave of `pairs` CTA pairs at a time
+    units = plan["tiles"]                       # tiles, one wave of `pairs` CTA pairs at a time
     blocks = -(-units // pairs) * plan["k_blocks"]     # the busiest pair's K blocks
-    t1, t4 = res["S1"]["us"], res["S4"]["us"]
-    c, latency = cost_model.fit(blocks, t1, t4)
-    pred = cost_model.predict_sweep(blocks, t1, t4, (2, 3))
-    return {"fit": "c and L per K block from S = 1 (B (L + c)) and S = 4 (B c), B = the busiest CTA pair's blocks",
+    t1, th = res["S1"]["us"], res[f"S{hi}"]["us"]
+    c, latency = cost_model.fit(blocks, t1, th)
+    pred = cost_model.predict_sweep(blocks, t1, th, mids)
+    return {"fit": f"c and L per K block from S = 1 (B (L + c)) and S = {hi} (B c), "
+                   "B = the busiest CTA pair's blocks",
             "blocks": blocks, "c_us": round(c, 4), "L_us": round(latency, 4),
             "saturation_S": round(cost_model.saturation_stages(c, latency), 2),
             **{f"S{s}": {"predicted_us": round(pred[s], 1), "measured_us": res[f"S{s}"]["us"],
-                         "measured_over_predicted": round(res[f"S{s}"]["us"] / pred[s], 3)} for s in (2, 3)}}
+                         "measured_over_predicted": round(res[f"S{s}"]["us"] / pred[s], 3)} for s in mids}}
+
+
+def peaks_library():
+    """The measurement kernels (_build/libpwspeaks.so, built with the library)."""
+    import ctypes
+    from pipelined_warp_specialized_gb300 import build as libbuild
+    lib = ctypes.CDLL(libbuild.PEAKS_PATH)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    lib.pws_peaks_imad.argtypes = [i32, i32, i32, vp, vp]
+    lib.pws_peaks_imad.restype = i32
+    lib.pws_peaks_empty.argtypes = [i32, i32, vp]
+    lib.pws_peaks_empty.restype = i32
+    lib.pws_peaks_imad_chains.restype = i32
+    return lib
+
+
+def s32_roofline(torch, stream, us, ops, grid_blocks=128, threads=256):
+    """The s32 path's two bounds, measured here: the CUDA-core peak of 32-bit
+    multiply-adds (each counted as 2 ops, like 2MNK) from a kernel of
+    independent mad.lo.u32 chains on every SM, and the launch floor, an
+    empty kernel with the s32 page problem's grid (8 x 16 blocks of 256
+    threads), launched the same way and replayed from a CUDA graph."""
+    lib = peaks_library()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    blocks, thr, iters = sms * 8, 256, 4096
+    call = lambda: lib.pws_peaks_imad(blocks, thr, iters, sink.data_ptr(), stream.cuda_stream)
+    ms = time_launches(call, 20, 5, torch, stream)
+    imads = blocks * thr * iters * lib.pws_peaks_imad_chains()
+    peak_tops = 2 * imads / ms / 1e9
+    floor_ms = time_graph(lambda st: lib.pws_peaks_empty(grid_blocks, threads, st.cuda_stream), torch)
+    return {"imad_peak_TOPS": round(peak_tops, 2),
+            "imad_peak_how": f"{blocks} blocks x {thr} threads x {iters} x {lib.pws_peaks_imad_chains()} "
+                             f"independent mad.lo.u32, 2 ops each, {ms * 1e3:.0f} us",
+            "frac_of_imad_peak": round(ops / (us * 1e-6) / 1e12 / peak_tops, 4),
+            "launch_floor_us": round(floor_ms * 1e3, 2),
+            "launch_floor_how": f"empty kernel, {grid_blocks} blocks x {threads} threads, programmatic "
+                                "dependent launch, CUDA-graph replay",
+            "over_launch_floor": round(us / (floor_ms * 1e3), 2)}
 
 
 def extra_configs(pws, torch, stream):
@@ -395,6 +436,7 @@ def extra_configs(pws, torch, stream):
     out[wl.name] = {"us": round(ms * 1e3, 2), "TOPS": round(wl.flops / ms / 1e9, 3),
                     "GB_s": round((wl.M * wl.K + wl.K * wl.N + wl.M * wl.N) * 4 / ms / 1e6, 1),
                     "us_eager": round(ms_eager * 1e3, 2), "timing": "CUDA-graph replay (us), eager calls (us_eager)"}
+    out[wl.name]["roofline"] = s32_roofline(torch, stream, ms * 1e3, wl.flops)
     ring = {}
     for s in range(2, 7):
         ms = time_graph(lambda st: pws.gemm_s32_nn_ring(a, b, c, stages=s, stream=st), torch)
@@ -444,10 +486,48 @@ def extra_configs(pws, torch, stream):
                 pairs = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count // 2
                 res["model"] = sweep_model(res, plan, pairs)
             out[name + ("/" + suffix if suffix else "")] = res
+        if name == "f16_nt_8192":
+            # the same sweep on one tile for every S (256 x 256 pairs; the
+            # default switches to the 256 x 512 tile for S <= 4), so each step
+            # of S changes the ring depth only, and the model fitted to S = 1
+            # and S = 6 predicts S = 2 .. 5
+            pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_NARROW_TILE)
+            try:
+                res = {"producer": "tma", "cta_group": 2}
+                for s in range(1, 7):
+                    ms = time_steady(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), torch, stream)
+                    res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
+                                    "tile": "256x256",
+                                    "timing": "0.25 s warm-up, then 0.25 s of back-to-back launches"}
+                plan_n = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), 6)
+            finally:
+                pws.gemm_set_debug_flags(0)
+            pairs = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count // 2
+            res["model"] = sweep_model(res, plan_n, pairs, hi=6)
+            out[name + "/same_tile_256x256"] = res
         del a, b, c
     out.update(concurrency_configs(pws, torch))
     out.update(per_launch_distribution(pws, torch, stream))
     return out
+
+
+def run_s32(args):
+    """Times gemm_s32_nn alone on the s32 workload (back-to-back launches on
+    one stream), e.g. to profile its kernel; the full bench reports it under
+    `configs` with its roofline."""
+    import torch
+    import pipelined_warp_specialized_gb300 as pws
+    pws.load_library()
+    stream = torch.cuda.current_stream()
+    wl = args.wl
+    a, b = torch.from_numpy(wl.lhs()).cuda(), torch.from_numpy(wl.rhs()).cuda()
+    c = torch.empty(wl.M, wl.N, dtype=torch.int32, device="cuda")
+    ms = time_launches(lambda: pws.gemm_s32_nn(a, b, c, stream=stream), args.steps, args.warmup, torch, stream)
+    if pws.gemm_device_status() != pws.GEMM_OK:
+        raise RuntimeError("device status after timing")
+    return {"metric": "s32 NN GEMM TOPS (eager launches)", "value": round(wl.flops / ms / 1e9, 3), "unit": "TOPS",
+            "us_per_launch": round(ms * 1e3, 2), "steps": args.steps, "warmup": args.warmup,
+            "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K}}
 
 
 def run_ours(args, world, rank, local):
@@ -473,6 +553,8 @@ def run_ours(args, world, rank, local):
     def step():
         pws.gemm_f16_nt(a, b, c, stages=S, stream=stream)
 
+    if args.tile == "narrow":
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_NARROW_TILE)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -504,6 +586,8 @@ def run_ours(args, world, rank, local):
     status = pws.gemm_device_status()
     if status != pws.GEMM_OK:
         raise RuntimeError(f"device status after timing: {pws.gemm_status_string(status)}")
+    plan = pws.gemm_f16_nt_plan(M, N, K, stages=S)
+    pws.gemm_set_debug_flags(0)
     ms = ms_total / args.steps
     value = world * flops / ms / 1e9          # TFLOP/s over all ranks
 
@@ -523,9 +607,9 @@ def run_ours(args, world, rank, local):
     long_region = ms_total > 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     achieved = flops / ms / 1e9
-    plan = pws.gemm_f16_nt_plan(M, N, K, stages=S)
     nw = plan["bn"] // (128 * plan["cta_group"])
-    roofline = {"bound": "tensor", "kernel": f"gemm_f16_nt_kernel<{plan['cta_group']},{S},{nw}>",
+    pk = 1 if plan["cta_group"] == 2 and plan["producer"] != 0 else 0
+    roofline = {"bound": "tensor", "kernel": f"gemm_f16_nt_kernel<{plan['cta_group']},{S},{nw},{pk}>",
                 "tile": f"{plan['bm']}x{plan['bn']}",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
@@ -535,7 +619,7 @@ def run_ours(args, world, rank, local):
                 "algorithmic_bytes_per_launch": int((M * K + N * K + M * N) * 2)}
 
     extras = None
-    if rank == 0 and world == 1 and not args.no_sweep and (M, N, K) == (8192, 8192, 8192):
+    if rank == 0 and world == 1 and not args.no_sweep and (M, N, K) == (8192, 8192, 8192) and args.tile == "auto":
         extras = extra_configs(pws, torch, stream)
 
     cpu = None
@@ -663,8 +747,12 @@ def main():
     ap.add_argument("--stages", type=int, default=4,
                     help="ring slots S of the timed GEMM (4: the wide 256x512 pair tile, the fastest "
                          "sustained configuration on GB300; 5 and 6 run the 256x256 tile)")
-    ap.add_argument("--workload", default="f16_nt_8192", choices=[k for k in inputs.WORKLOADS if k.startswith("f16")],
-                    help="the seeded f16 workload of the timed GEMM")
+    ap.add_argument("--workload", default="f16_nt_8192", choices=list(inputs.WORKLOADS),
+                    help="the seeded workload of the timed GEMM (the s32 one times gemm_s32_nn alone, "
+                         "for profiling)")
+    ap.add_argument("--tile", choices=["auto", "narrow"], default="auto",
+                    help="narrow: the 256x256 pair tile for every S (GEMM_DEBUG_FORCE_NARROW_TILE), as in "
+                         "the same-tile S sweep")
     ap.add_argument("--shape", default=None, help="M,N,K override (uniform [-1,1) inputs, seed 5)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-workload timings")
     ap.add_argument("--no-e2e", action="store_true")
@@ -681,6 +769,11 @@ def main():
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     world, rank, local = dist_env()
+    if args.wl.kind == "s32_nn":
+        if args.impl == "reference" or world > 1:
+            ap.error("the s32 workload is timed alone, on one GPU, for profiling")
+        print(json.dumps(run_s32(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, world, rank)
     else:

@@ -1,4 +1,5 @@
-"""Builds the C-ABI shared library ``_build/libpwsgemm.so`` for sm_103a with nvcc.
+"""Builds the C-ABI shared library ``_build/libpwsgemm.so`` for sm_103a with nvcc,
+and the measurement kernels bench.py uses (``_build/libpwspeaks.so``).
 
 Each translation unit compiles in parallel; the objects are linked into one
 shared library (CUDA runtime linked statically, no libcuda link: the driver's
@@ -20,8 +21,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpwsgemm.so")
+PEAKS_PATH = os.path.join(OUT_DIR, "libpwspeaks.so")
 
 SOURCES = ["runtime.cu", "gemm_s32_nn.cu", "gemm_f16_nt.cu"]
+PEAKS_SOURCES = ["peaks.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ptx.cuh", "internal.h")] + [os.path.join(INCLUDE, "pwsgemm.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -42,10 +45,10 @@ def _flags(verbose: bool) -> list:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+    if not os.path.exists(LIB_PATH) or not os.path.exists(PEAKS_PATH):
         return True
-    t = os.path.getmtime(LIB_PATH)
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [os.path.abspath(__file__)]
+    t = min(os.path.getmtime(LIB_PATH), os.path.getmtime(PEAKS_PATH))
+    deps = [os.path.join(CSRC, s) for s in SOURCES + PEAKS_SOURCES] + HEADERS + [os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
@@ -62,21 +65,22 @@ def build(force: bool = False, verbose: bool = False) -> str:
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES + PEAKS_SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES + PEAKS_SOURCES))
     failed = [(s, r) for s, _, r in results if r.returncode != 0]
     for s, _, r in results:
         if verbose or r.returncode != 0:
             sys.stderr.write(f"--- {s}\n{r.stdout}{r.stderr}")
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(s for s, _ in failed))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for _, o, _ in results]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("link failed")
-    os.replace(tmp, LIB_PATH)
+    for path, srcs in ((LIB_PATH, SOURCES), (PEAKS_PATH, PEAKS_SOURCES)):
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for s, o, _ in results if s in srcs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError("link failed")
+        os.replace(tmp, path)
     return LIB_PATH
 
 
