@@ -38,8 +38,13 @@
  *   - M == 0 or N == 0 is a successful no-op.  K == 0 writes zeros to `out`
  *     (the empty sum).
  *   - A wait inside a kernel that exceeds the wait limit (see
- *     gemm_set_wait_timeout_ns) records GEMM_ERR_TIMEOUT in a device status
- *     word and the kernel returns; gemm_device_status() reads and clears it.
+ *     gemm_set_wait_timeout_ns) records GEMM_ERR_TIMEOUT in the status word
+ *     of the call's stream and the kernel returns; gemm_device_status(stream)
+ *     reads and clears it.
+ *   - Per-device state (the status words, the no-alloc array's address, the
+ *     kernels' shared-memory settings) is set up on the first call on a
+ *     device and kept for the life of the process: after cudaDeviceReset the
+ *     library must not be called again in that process.
  */
 #ifndef PWSGEMM_H_
 #define PWSGEMM_H_
@@ -208,15 +213,22 @@ int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, 
 
 /*
  * gemm_device_status -- synchronizes `stream`, then returns and clears the
- * device status word of the current device: GEMM_OK, or GEMM_ERR_TIMEOUT if a
- * bounded wait inside any kernel of this library expired since the last call.
- * Returns GEMM_ERR_LAUNCH if the synchronization itself failed.
+ * status word of that stream on the current device: GEMM_OK, or
+ * GEMM_ERR_TIMEOUT if a bounded wait inside a kernel of this library launched
+ * on `stream` expired since the last call for it.  Returns GEMM_ERR_LAUNCH if
+ * the synchronization itself failed.
  *
  * Every device-side wait of the pipelines (mbarrier phase waits) gives up
  * after the wait limit; the waiting role then records the timeout, drains
  * what it has in flight and the kernel returns, so the CUDA context stays
  * usable.  This is the device analogue of the deadlock the Croqtile tutorial
  * ch.6 describes for a missing empty seed ("消费者路径").
+ *
+ * Each stream has its own word: a timeout in a call on one stream is neither
+ * seen nor cleared by gemm_device_status on another.  The library keeps words
+ * for the first 63 streams it sees on each device (keyed by the stream
+ * handle, for the life of the process); later streams share one more word.
+ * A handle reused by a new stream inherits the old stream's word.
  */
 int gemm_device_status(cudaStream_t stream);
 
@@ -265,6 +277,11 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *       their partial sums to the peer CTA send nothing and never signal it;
  *       used to test that the owners' wait for them ends in GEMM_ERR_TIMEOUT
  *       while the rest of the cluster finishes normally.
+ *   GEMM_DEBUG_FORCE_DOUBLE_SLOT   : where the single-CTA tile is fed by TMA
+ *       without the K split and stages <= 3, use ring slots of several
+ *       64-wide K boxes (three for stages <= 2, two for 3) even when the
+ *       tiles exceed one wave.
+ *   GEMM_DEBUG_NO_DOUBLE_SLOT      : never use multi-box slots.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -279,7 +296,9 @@ enum {
     GEMM_DEBUG_SKIP_ACC_SEED = 256u,
     GEMM_DEBUG_NO_KSPLIT = 512u,
     GEMM_DEBUG_FORCE_KSPLIT = 1024u,
-    GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048u
+    GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048u,
+    GEMM_DEBUG_FORCE_DOUBLE_SLOT = 4096u,
+    GEMM_DEBUG_NO_DOUBLE_SLOT = 8192u
 };
 int gemm_set_debug_flags(unsigned flags);
 
@@ -309,14 +328,16 @@ int gemm_set_scratch_pool(int enable);
  * arguments, without touching a device (host logic only).  Validates the
  * arguments exactly as gemm_f16_nt does and returns the same status.
  *   plan[0] tile rows per CTA group (BM)      plan[1] tile columns (BN)
- *   plan[2] K per ring slot (BK)              plan[3] CTAs per tile (1 or 2)
+ *   plan[2] K per ring slot (64; 192 or 128 for multi-box slots)
+ *   plan[3] CTAs per tile (1 or 2)
  *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy,
  *           2 = tensor memory accelerator on an aligned scratch copy
  *           (gemm_set_scratch_pool), 3 = realigning loads in place
  *   plan[5] copy granularity in bytes (16 for TMA, else 8, 4 or 2)
  *   plan[6] output store: 0 = tensor memory accelerator, 1 = plain stores
  *   plan[7] dynamic shared memory bytes per CTA
- *   plan[8] number of output tiles        plan[9] number of K blocks
+ *   plan[8] number of output tiles
+ *   plan[9] number of K blocks (of plan[2] columns each)
  *   plan[10] CTAs summing parts of K per tile: 1, or 2 (the K split)
  * `plan` must hold 11 int64 values.
  */

@@ -41,6 +41,8 @@ GEMM_DEBUG_SKIP_ACC_SEED = 256
 GEMM_DEBUG_NO_KSPLIT = 512
 GEMM_DEBUG_FORCE_KSPLIT = 1024
 GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048
+GEMM_DEBUG_FORCE_DOUBLE_SLOT = 4096
+GEMM_DEBUG_NO_DOUBLE_SLOT = 8192
 
 _lib = None
 

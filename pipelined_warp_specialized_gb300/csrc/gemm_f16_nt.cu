@@ -157,14 +157,17 @@ struct Shape {
     static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 };
 
-// Shared-memory carve-up (offsets from a 1024-byte aligned base).  Slot s
-// holds A at A + s * A_SLOT and its NW B boxes at B + s * NW * B_SLOT.
-template <int S, int NW = 1>
+// Shared-memory carve-up (offsets from a 1024-byte aligned base).  A slot
+// holds KB 64-wide K boxes of each operand: slot s holds A box j at
+// A + s * A_STRIDE + j * A_SLOT and B box j at B + s * B_STRIDE + j * B_SLOT,
+// or, for the wide tile (KB = 1), its NW B boxes at B + s * B_STRIDE + h * B_SLOT.
+template <int S, int NW = 1, int KB = 1>
 struct Layout {
-    static constexpr int B_STRIDE = NW * B_SLOT;
+    static constexpr int A_STRIDE = KB * A_SLOT;
+    static constexpr int B_STRIDE = NW * KB * B_SLOT;
     static constexpr int A = 0;
-    static constexpr int B = S * A_SLOT;
-    static constexpr int EPI = S * (A_SLOT + B_STRIDE);
+    static constexpr int B = S * A_STRIDE;
+    static constexpr int EPI = S * (A_STRIDE + B_STRIDE);
     static constexpr int BAR = EPI + EPI_BYTES;
     static constexpr int FULL = BAR;
     static constexpr int EMPTY = FULL + 8 * S;
@@ -605,14 +608,19 @@ __device__ void realign_producer(const Params& p, const Waiter& W, uint32_t sA, 
 // realigning producer), PK = 0: with one (TMA).  Single-CTA kernels serve
 // every producer with one bound; a CTA pair has a kernel per producer kind,
 // so the TMA one keeps the registers eight producer warps would take.
-template <int CG, int S, int NW, int PK>
+//
+// KB = 2 or 3 (single-CTA tile, TMA): each slot holds KB 64-wide K boxes of
+// each operand, so a latency-bound K loop runs 1/KB as many slot round
+// trips; the multiplies keep their K order, so the result bits do not change.
+template <int CG, int S, int NW, int PK, int KB = 1>
 __global__ void __launch_bounds__(((CG == 1 || PK == 1 ? COPY_WARPS : 1) + 1 + epi_warps<NW, PK>()) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ Params p) {
     static_assert(NW == 1 || CG == 2, "the wide tile is a CTA-pair tile");
     using SH = Shape<CG, NW>;
-    using L = Layout<S, NW>;
+    using L = Layout<S, NW, KB>;
+    static_assert(KB == 1 || (CG == 1 && NW == 1 && PK == 0), "multi-box slots: single-CTA TMA tile only");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     const uint32_t raw = smem_u32(smem_raw);
@@ -719,8 +727,17 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     const uint32_t bytes = NW == 1 && halfw ? A_SLOT + B_SLOT / 2 : A_SLOT + nbox * B_SLOT;
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!W.wait(bEMPTY + 8 * stage, phase)) { ok = false; break; }
-                        const uint32_t a_dst = sA + stage * A_SLOT, b_dst = sB + stage * L::B_STRIDE;
-                        if constexpr (CG == 1) {
+                        const uint32_t a_dst = sA + stage * L::A_STRIDE, b_dst = sB + stage * L::B_STRIDE;
+                        if constexpr (CG == 1 && KB > 1) {
+                            // the slot's boxes inside K (a box wholly past K is neither
+                            // loaded nor multiplied)
+                            const int nk = min(KB, (p.K - kb * KB * BK + BK - 1) / BK);
+                            mbar_arrive_expect_tx(bFULL + 8 * stage, static_cast<uint32_t>(nk) * bytes);
+                            for (int j = 0; j < nk; ++j) {
+                                tma_load_2d(a_dst + j * A_SLOT, &tmA, (kb * KB + j) * BK, m_cta, bFULL + 8 * stage);
+                                tma_load_2d(b_dst + j * B_SLOT, tb, (kb * KB + j) * BK, n_cta, bFULL + 8 * stage);
+                            }
+                        } else if constexpr (CG == 1) {
                             mbar_arrive_expect_tx(bFULL + 8 * stage, bytes);
                             tma_load_2d(a_dst, &tmA, kb * BK, m_cta, bFULL + 8 * stage);
                             tma_load_2d(b_dst, tb, kb * BK, n_cta, bFULL + 8 * stage);
@@ -756,12 +773,12 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 }
             }
         } else if (p.producer == kProducerRealign) {
-            if constexpr (CG == 1 || PK == 1) {
+            if constexpr ((CG == 1 || PK == 1) && KB == 1) {
                 const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
                 realign_producer<CG, NW, S>(p, W, sA, sB, bFULL, bEMPTY, sPROGRESS, cluster_id, num_clusters, kb0,
                                             kb1, rank, warp, lane);
             }
-        } else if constexpr (CG == 1) {
+        } else if constexpr (CG == 1 && KB == 1) {
             // cp.async producer (single CTA only): COPY_WARPS warps fill the swizzled slot
             const Waiter W{p.timeout_ns, abort_flag, p.status, kStatusRoleProducer};
             if (p.copy_bytes == 8)
@@ -821,12 +838,18 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         tc_fence_after_sync();
                         if (p.producer == kProducerCopy) fence_proxy_async_smem();
                         for (int j = 0; j < nb; ++j) {
-                            const uint64_t adesc = make_sdesc(sA + st[j] * A_SLOT);
-                            const uint64_t bdesc = make_sdesc(sB + st[j] * B_SLOT);
 #pragma unroll
-                            for (int k = 0; k < BK / UMMA_K; ++k) {
-                                // +32 bytes of K per step: +2 in the (address >> 4) field
-                                tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, (kb + j) != kb0 || k != 0);
+                            for (int bx = 0; bx < KB; ++bx) {
+                                // a box wholly past K was not loaded (two-box slots)
+                                if (KB > 1 && ((kb + j) * KB + bx) * BK >= p.K) break;
+                                const uint64_t adesc = make_sdesc(sA + st[j] * L::A_STRIDE + bx * A_SLOT);
+                                const uint64_t bdesc = make_sdesc(sB + st[j] * L::B_STRIDE + bx * B_SLOT);
+#pragma unroll
+                                for (int k = 0; k < BK / UMMA_K; ++k) {
+                                    // +32 bytes of K per step: +2 in the (address >> 4) field
+                                    tc_mma_f16<CG>(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                                                   (kb + j) != kb0 || bx != 0 || k != 0);
+                                }
                             }
                         }
                         issued_any = true;
@@ -1378,6 +1401,7 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0;
     int smem = 0;
     int ksplit = 1;             // 2: two CTAs (a cluster) per single-CTA tile, one K half each
+    int kb = 1;                 // 64-wide K boxes per ring slot (2 or 3: single-CTA TMA tile, S <= 3)
 };
 
 // Fewest K blocks for which small single-CTA GEMMs split K over two CTAs.
@@ -1389,7 +1413,9 @@ constexpr int64_t kPooledRowAlign = 64;
 // The wide tile's 48 KB slots fit the shared memory up to this many stages.
 constexpr int WIDE_MAX_STAGES = 4;
 
-int smem_for(int stages, int nw) {
+int smem_for(int stages, int nw, int kb = 1) {
+    if (kb == 3) return stages == 1 ? Layout<1, 1, 3>::DYN : Layout<2, 1, 3>::DYN;
+    if (kb == 2) return Layout<3, 1, 2>::DYN;
     if (nw == 2) {
         switch (stages) {
             case 1: return Layout<1, 2>::DYN;
@@ -1519,7 +1545,6 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     pl.tiles_n = static_cast<int>((N + tile_n - 1) / tile_n);
     pl.num_tiles = pl.tiles_m * pl.tiles_n;
     pl.num_kb = static_cast<int>((K + BK - 1) / BK);
-    pl.smem = smem_for(stages, pl.nw);
     // K split: where single-CTA tiles leave at least half of the SMs idle and
     // K is long, a cluster of two CTAs computes each tile, one K half each.
     // Small GEMMs are bound by the chain of K blocks through the ring (each
@@ -1534,6 +1559,17 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
         const bool forced = flags & GEMM_DEBUG_FORCE_KSPLIT;
         if (pl.num_kb >= (forced ? 2 : kKSplitMinBlocks) && (forced || 2ll * pl.num_tiles <= num_sms)) pl.ksplit = 2;
     }
+    // Multi-box slots: on the single-CTA TMA tile with up to three slots,
+    // when the tiles fit in one wave, so that each CTA's chain of K blocks
+    // through the ring is what bounds the call: three boxes per slot for one
+    // or two slots, two for three (the most that fit in shared memory).
+    // Each element keeps its K order: the result is the same for every choice.
+    if (pl.cg == 1 && pl.ksplit == 1 && pl.producer == kProducerTma && stages <= 3 && pl.num_kb >= 2 &&
+        !(flags & GEMM_DEBUG_NO_DOUBLE_SLOT) &&
+        ((flags & GEMM_DEBUG_FORCE_DOUBLE_SLOT) || pl.num_tiles <= num_sms))
+        pl.kb = stages <= 2 ? 3 : 2;
+    pl.num_kb = static_cast<int>((K + BK * pl.kb - 1) / (BK * pl.kb));
+    pl.smem = smem_for(stages, pl.nw, pl.kb);
     return pl;
 }
 
@@ -1545,11 +1581,11 @@ inline int block_threads(const Plan& pl) {
 // Sets the kernel's shared-memory limit (once per device) and returns how
 // many CTA groups (pairs or single CTAs) can be resident at once: the size of
 // the persistent grid.  0 on failure.
-template <int CG, int S, int NW, int PK>
+template <int CG, int S, int NW, int PK, int KB = 1>
 int capacity(const DeviceInfo& info, int threads) {
-    auto kern = gemm_f16_nt_kernel<CG, S, NW, PK>;
-    constexpr int smem = Layout<S, NW>::DYN;
-    static_assert(Layout<S, NW>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
+    auto kern = gemm_f16_nt_kernel<CG, S, NW, PK, KB>;
+    constexpr int smem = Layout<S, NW, KB>::DYN;
+    static_assert(Layout<S, NW, KB>::BYTES <= 232448, "ring + staging exceed the per-block shared memory");
     // per-device caches; concurrent first calls from several host threads
     // compute and store the same values
     static std::atomic<int> configured[64] = {};
@@ -1603,6 +1639,14 @@ inline int pk_of(const Plan& pl) { return pl.cg == 2 && pl.producer != kProducer
 
 int capacity_of(const Plan& pl, int stages, const DeviceInfo& info) {
     const int threads = block_threads(pl);
+    if (pl.kb > 1) {
+        switch (stages) {
+            case 1: return capacity<1, 1, 1, 0, 3>(info, threads);
+            case 2: return capacity<1, 2, 1, 0, 3>(info, threads);
+            case 3: return capacity<1, 3, 1, 0, 2>(info, threads);
+        }
+        return 0;
+    }
     if (pl.cg == 1) return capacity_for<1, 1, 0>(stages, info, threads);
     if (pk_of(pl))
         return pl.nw == 2 ? capacity_for<2, 2, 1>(stages, info, threads) : capacity_for<2, 1, 1>(stages, info, threads);
@@ -1611,17 +1655,17 @@ int capacity_of(const Plan& pl, int stages, const DeviceInfo& info) {
 
 // Launches the persistent grid: one CTA group per work unit, at most as many
 // as can be resident.
-template <int CG, int S, int NW, int PK>
+template <int CG, int S, int NW, int PK, int KB = 1>
 int launch(const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
            const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
-    auto kern = gemm_f16_nt_kernel<CG, S, NW, PK>;
+    auto kern = gemm_f16_nt_kernel<CG, S, NW, PK, KB>;
     const int threads = block_threads(pl);
-    const int cap = capacity<CG, S, NW, PK>(info, threads);
+    const int cap = capacity<CG, S, NW, PK, KB>(info, threads);
     if (cap <= 0) return GEMM_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
     cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = Layout<S, NW>::DYN;
+    cfg.dynamicSmemBytes = Layout<S, NW, KB>::DYN;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -1660,6 +1704,14 @@ int launch_stages(int stages, const Plan& pl, const DeviceInfo& info, const CUte
 
 int launch_plan(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
                 const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
+    if (pl.kb > 1) {
+        switch (stages) {
+            case 1: return launch<1, 1, 1, 0, 3>(pl, info, ta, tb, tbh, tc, p, stream);
+            case 2: return launch<1, 2, 1, 0, 3>(pl, info, ta, tb, tbh, tc, p, stream);
+            case 3: return launch<1, 3, 1, 0, 2>(pl, info, ta, tb, tbh, tc, p, stream);
+        }
+        return GEMM_ERR_UNSUPPORTED_STAGES;
+    }
     if (pl.cg == 1) return launch_stages<1, 1, 0>(stages, pl, info, ta, tb, tbh, tc, p, stream);
     if (pk_of(pl))
         return pl.nw == 2 ? launch_stages<2, 2, 1>(stages, pl, info, ta, tb, tbh, tc, p, stream)
@@ -1682,7 +1734,7 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
                               pws::scratch_pool_enabled());
     plan[0] = 128 * pl.cg;
     plan[1] = 128 * pl.cg * pl.nw;
-    plan[2] = BK;
+    plan[2] = BK * pl.kb;
     plan[3] = pl.cg;
     plan[4] = pl.repack ? 2 : pl.producer;       // 0 TMA, 1 cp.async, 2 repack + TMA, 3 realigning loads
     plan[5] = pl.copy_bytes;
@@ -1744,7 +1796,7 @@ int run_plan(const Plan& pl, const DeviceInfo& info, int64_t M, int64_t N, int64
     p.lhs = static_cast<const __half*>(lhs);
     p.rhs = static_cast<const __half*>(rhs);
     p.out = static_cast<__half*>(out);
-    p.status = info.status;
+    p.status = status_word(info, stream);
     p.full_units = pl.num_tiles;
     p.split = 0;
     p.total_units = pl.num_tiles;

@@ -17,17 +17,25 @@ enum : unsigned {
     kStatusRoleEpilogue = 1u << 10,
 };
 
+// Status words per device: slot 0 is shared by streams beyond the first
+// kStatusSlots - 1 seen on the device.
+constexpr int kStatusSlots = 64;
+
 struct DeviceInfo {
     int device = -1;
     int cc_major = 0, cc_minor = 0;
     int num_sms = 0;
     int max_smem_optin = 0;
-    unsigned* status = nullptr;   // device address of this device's status word
+    unsigned* status = nullptr;   // device address of this device's kStatusSlots status words
 };
 
 // Fills `info` for the current device.  Returns GEMM_OK,
 // GEMM_ERR_UNSUPPORTED_ARCH (not compute capability 10.3) or GEMM_ERR_LAUNCH.
 int current_device(DeviceInfo* info);
+
+// The status word a launch on `stream` records its timeouts in, and the one
+// gemm_device_status(stream) reads and clears.
+unsigned* status_word(const DeviceInfo& info, cudaStream_t stream);
 
 uint64_t wait_timeout_ns();
 unsigned debug_flags();

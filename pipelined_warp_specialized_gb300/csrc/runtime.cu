@@ -11,9 +11,11 @@ namespace pws {
 
 namespace {
 
-// One status word per device (a __device__ variable exists once in every
-// context that loads this module).  Kernels OR status bits into it.
-__device__ unsigned g_status_word;
+// Status words: kStatusSlots per device (a __device__ variable exists once in
+// every context that loads this module).  A launch gets the word of its
+// stream's slot and its kernels OR status bits into it, so that a timeout is
+// reported to, and cleared by, the stream whose call had it.
+__device__ unsigned g_status_words[kStatusSlots];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -66,7 +68,7 @@ int current_device(DeviceInfo* info) {
                 return GEMM_ERR_LAUNCH;
             if (d.cc_major == 10 && d.cc_minor == 3) {
                 void* p = nullptr;
-                if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return GEMM_ERR_LAUNCH;
+                if (cudaGetSymbolAddress(&p, g_status_words) != cudaSuccess) return GEMM_ERR_LAUNCH;
                 d.status = static_cast<unsigned*>(p);
             }
             g_info[dev] = d;
@@ -76,6 +78,36 @@ int current_device(DeviceInfo* info) {
     }
     if (info->cc_major != 10 || info->cc_minor != 3) return GEMM_ERR_UNSUPPORTED_ARCH;
     return GEMM_OK;
+}
+
+namespace {
+// Stream -> status slot, per device: open addressing over slots
+// 1 .. kStatusSlots-1 keyed by the stream handle (stored + 1, so 0 marks a
+// free entry).  Entries are never evicted; once every slot is taken, further
+// streams share slot 0.  A handle reused by a later stream inherits its slot.
+std::mutex g_slot_mu;
+uintptr_t g_slot_key[kMaxDevices][kStatusSlots] = {};
+}  // namespace
+
+int status_slot(int device, cudaStream_t stream) {
+    if (device < 0 || device >= kMaxDevices) return 0;
+    const uintptr_t key = reinterpret_cast<uintptr_t>(stream) + 1u;
+    const int n = kStatusSlots - 1;
+    int h = static_cast<int>(((key >> 4) * 0x9E3779B97F4A7C15ull) >> 40) % n;
+    std::lock_guard<std::mutex> lk(g_slot_mu);
+    for (int i = 0; i < n; ++i, h = h + 1 == n ? 0 : h + 1) {
+        uintptr_t& e = g_slot_key[device][1 + h];
+        if (e == key) return 1 + h;
+        if (e == 0) {
+            e = key;
+            return 1 + h;
+        }
+    }
+    return 0;
+}
+
+unsigned* status_word(const DeviceInfo& info, cudaStream_t stream) {
+    return info.status ? info.status + status_slot(info.device, stream) : nullptr;
 }
 
 uint64_t wait_timeout_ns() {
@@ -158,13 +190,12 @@ int gemm_device_status(cudaStream_t stream) {
     const int rc = pws::current_device(&info);
     if (rc != GEMM_OK) return rc;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    unsigned* w = pws::status_word(info, stream);
     unsigned word = 0;
-    if (cudaMemcpy(&word, info.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return GEMM_ERR_LAUNCH;
+    if (cudaMemcpy(&word, w, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_LAUNCH;
     if (word) {
         const unsigned zero = 0;
-        if (cudaMemcpy(info.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
-            return GEMM_ERR_LAUNCH;
+        if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GEMM_ERR_LAUNCH;
     }
     return (word & pws::kStatusTimeout) ? GEMM_ERR_TIMEOUT : GEMM_OK;
 }
@@ -198,7 +229,8 @@ int gemm_set_debug_flags(unsigned flags) {
                            GEMM_DEBUG_FORCE_PAIR_TILE | GEMM_DEBUG_NO_SPLIT |
                            GEMM_DEBUG_FORCE_NARROW_TILE | GEMM_DEBUG_FORCE_WIDE_TILE |
                            GEMM_DEBUG_SKIP_ACC_SEED | GEMM_DEBUG_NO_KSPLIT | GEMM_DEBUG_FORCE_KSPLIT |
-                           GEMM_DEBUG_SKIP_KSPLIT_SEND;
+                           GEMM_DEBUG_SKIP_KSPLIT_SEND | GEMM_DEBUG_FORCE_DOUBLE_SLOT |
+                           GEMM_DEBUG_NO_DOUBLE_SLOT;
     if (flags & ~known) return GEMM_ERR_INVALID_ARG;
     pws::g_flags.store(flags, std::memory_order_relaxed);
     return GEMM_OK;

@@ -123,7 +123,7 @@ def test_s32_ring_argument_checks_return_before_launch(lib, args, want):
 
 
 def test_debug_flags_and_timeout_setters(lib):
-    assert lib.gemm_set_debug_flags(1 << 12) == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_debug_flags(1 << 14) == pws.GEMM_ERR_INVALID_ARG
     assert lib.gemm_set_debug_flags(0) == pws.GEMM_OK
     assert lib.gemm_set_wait_timeout_ns(0) == pws.GEMM_OK
 
@@ -202,9 +202,15 @@ def test_plan_sum_order_never_depends_on_stages(lib):
         for N in dims:
             for K in ks:
                 plans = [pws.gemm_f16_nt_plan(M, N, K, stages=s) for s in range(1, 7)]
-                assert len({(p["cta_group"], p["k_split"], p["bk"]) for p in plans}) == 1, (M, N, K)
+                assert len({(p["cta_group"], p["k_split"]) for p in plans}) == 1, (M, N, K)
                 for s, p in enumerate(plans, start=1):
                     assert p["bn"] != 512 or s <= 4, (M, N, K, s)            # the wide tile needs <= 4 slots
+                    # multi-box slots (192 or 128 K columns per slot,
+                    # multiplied in the same K order) only on the single-CTA
+                    # tile, without the K split, with at most 3 slots
+                    assert p["bk"] == 64 or (p["bk"] == (192 if s <= 2 else 128) and s <= 3
+                                             and p["cta_group"] == 1 and p["k_split"] == 1), (M, N, K, s)
+                    assert p["k_blocks"] == -(-K // p["bk"]), (M, N, K, s)
                     assert p["k_split"] == 1 or p["cta_group"] == 1, (M, N, K)
                     assert p["k_split"] == 1 or p["k_blocks"] >= 32, (M, N, K)
 

@@ -166,3 +166,40 @@ def test_long_k_loops_outlast_a_short_wait_limit(M, N, K, flags, want):
     ref = oracle.gemm_f16_nt_f64(a_np, b_np)
     got = out.cpu().numpy().view(np.uint16)
     assert np.array_equal(got, oracle.f64_to_f16(ref)), int((got != oracle.f64_to_f16(ref)).sum())
+
+
+def test_timeouts_are_reported_to_their_own_stream():
+    # A call that deadlocks (no empty seed, 0.2 s limit) on one stream beside
+    # a normal call on another: each stream's status word holds only its own
+    # call's outcome, so the normal stream reads GEMM_OK -- even while the
+    # other stream's kernel is still waiting out its limit -- and the
+    # deadlocked one reads GEMM_ERR_TIMEOUT once, then GEMM_OK.
+    M, N, K = 256, 256, 256
+    a_np = inputs.uniform_f16(9, 0, (M, K))
+    b_np = inputs.uniform_f16(9, 1, (N, K))
+    a = torch.from_numpy(a_np).cuda()
+    b = torch.from_numpy(b_np).cuda()
+    s_bad, s_good = torch.cuda.Stream(), torch.cuda.Stream()
+    out_bad = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    out_good = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    torch.cuda.synchronize()
+    assert pws.gemm_device_status(s_bad) == pws.GEMM_OK and pws.gemm_device_status(s_good) == pws.GEMM_OK
+    pws.gemm_set_wait_timeout_ns(200_000_000)
+    try:
+        pws.gemm_set_debug_flags(pws.GEMM_DEBUG_SKIP_EMPTY_SEED)
+        try:
+            pws.gemm_f16_nt(a, b, out_bad, stages=2, stream=s_bad)
+        finally:
+            pws.gemm_set_debug_flags(0)
+        pws.gemm_f16_nt(a, b, out_good, stages=2, stream=s_good)
+        assert pws.gemm_device_status(s_good) == pws.GEMM_OK        # synchronizes s_good only
+        assert pws.gemm_device_status(s_bad) == pws.GEMM_ERR_TIMEOUT
+        assert pws.gemm_device_status(s_bad) == pws.GEMM_OK         # cleared
+        assert pws.gemm_device_status(s_good) == pws.GEMM_OK
+        assert pws.gemm_device_status() == pws.GEMM_OK               # the current stream's own word
+    finally:
+        pws.gemm_set_debug_flags(0)
+        pws.gemm_set_wait_timeout_ns(0)
+    torch.cuda.synchronize()
+    res = oracle.check_f16(out_good.cpu().numpy(), oracle.gemm_f16_nt_f64(a_np, b_np), K)
+    assert res["ok"], res

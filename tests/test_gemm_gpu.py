@@ -184,12 +184,16 @@ def test_f16_stage_counts_bitwise_identical(flags):
 @pytest.mark.parametrize("M,N,K", [
     (2560, 2560, 256),      # wide tile for S <= 2, 256 x 256 for S >= 3: the same bits
     (2048, 2048, 512),      # the pair tile by wave count (64 pair tiles against 256 single)
-    (1024, 1152, 2100),     # the K split on repacked operands
+    (1024, 1152, 2100),     # the K split, the operands read in place
+    (1024, 1024, 1024),     # multi-box slots (192 / 128 K columns) for S <= 3, one box for S >= 4
+    (700, 900, 1000),       # multi-box slots, the last slot's later boxes past K (K = 1000)
+    (300, 260, 136),        # multi-box slots, the last slot's last box partly inside K
 ])
 def test_f16_stage_counts_bitwise_identical_where_the_plan_changes(M, N, K):
     a = inputs.uniform_f16(M + K, 0, (M, K))
     b = inputs.uniform_f16(M + K, 1, (N, K))
-    tiles = {(p["bm"], p["bn"], p["k_split"]) for p in (pws.gemm_f16_nt_plan(M, N, K, stages=s) for s in range(1, 7))}
+    tiles = {(p["bm"], p["bn"], p["bk"], p["k_split"])
+             for p in (pws.gemm_f16_nt_plan(M, N, K, stages=s) for s in range(1, 7))}
     outs = [run_f16(a, b, s) for s in range(1, 7)]
     for s in range(1, 6):
         assert np.array_equal(outs[s].view(np.uint16), outs[0].view(np.uint16)), f"S={s + 1} differs ({tiles})"
@@ -426,6 +430,28 @@ def test_f16_unaligned_every_row_alignment(offset):
     # every tile sums each element over K in the same order: the same bits
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("M,N,K,S,extra", [
+    (1024, 1024, 1024, 2, 0),   # the 1024^3 workload: 64 tiles as 128 half-width units (tail split)
+    (1000, 1100, 1090, 3, POOL),    # TMA on the repacked copy; the last slot's second box 2 columns deep
+    (2048, 2048, 200, 1, pws.GEMM_DEBUG_FORCE_SOLO_TILE),    # 256 tiles: more than one wave
+    (129, 77, 64, 2, 0),        # a single K block: one box per slot either way
+])
+def test_f16_two_box_slots_bitwise_equal_one_box(M, N, K, S, extra):
+    a = inputs.uniform_f16(90, 0, (M, K))
+    b = inputs.uniform_f16(90, 1, (N, K))
+    pws.gemm_set_debug_flags((pws.GEMM_DEBUG_FORCE_DOUBLE_SLOT | extra) & ~POOL)
+    pws.gemm_set_scratch_pool(bool(extra & POOL))
+    try:
+        bk = pws.gemm_f16_nt_plan(M, N, K, stages=S)["bk"]
+    finally:
+        pws.gemm_set_debug_flags(0)
+        pws.gemm_set_scratch_pool(False)
+    assert bk == (64 if K <= 64 else (192 if S <= 2 else 128))
+    outs = [run_f16(a, b, S, f | extra) for f in (pws.GEMM_DEBUG_FORCE_DOUBLE_SLOT, pws.GEMM_DEBUG_NO_DOUBLE_SLOT)]
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert_f16_ok(outs[0], oracle.gemm_f16_nt_f64(a, b), K)
 
 
 @pytest.mark.parametrize("M,N,K,S,flags,want", [
