@@ -554,14 +554,6 @@ __device__ __forceinline__ bool realign_unit(const Params& p, const Waiter& W, u
     return true;
 }
 
-// The unit's K loop for rows whose starts are all 4-byte aligned (K even,
-// both bases 4-byte aligned; the shifts are then 0, 4, 8 or 12 bytes).  A
-// lane loads its chunk where it lies, as one 16-byte, two 8-byte or four
-// 4-byte loads by the class's alignment (a warp-uniform choice), so it needs
-// neither the next block nor a shift, and 4 registers per operation: enough
-// to load K block k + 1 while K block k is written.  Each load holds a byte of
-// its row inside K (the K tail is masked afterwards), so none leaves the
-// operand's pages.
 template <int CG, int NW, int S>
 __device__ void realign_producer(const Params& p, const Waiter& W, uint32_t sA, uint32_t sB, uint32_t bFULL,
                                  uint32_t bEMPTY, uint32_t progress, int cluster_id, int num_clusters, int kb0,
