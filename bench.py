@@ -555,6 +555,7 @@ def run_ours(args, world, rank, local):
 
     if args.tile == "narrow":
         pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_NARROW_TILE)
+    pws.gemm_set_scratch_pool(args.scratch_pool)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -586,8 +587,9 @@ def run_ours(args, world, rank, local):
     status = pws.gemm_device_status()
     if status != pws.GEMM_OK:
         raise RuntimeError(f"device status after timing: {pws.gemm_status_string(status)}")
-    plan = pws.gemm_f16_nt_plan(M, N, K, stages=S)
+    plan = pws.gemm_f16_nt_plan(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), S)
     pws.gemm_set_debug_flags(0)
+    pws.gemm_set_scratch_pool(False)
     ms = ms_total / args.steps
     value = world * flops / ms / 1e9          # TFLOP/s over all ranks
 
@@ -609,7 +611,8 @@ def run_ours(args, world, rank, local):
     achieved = flops / ms / 1e9
     nw = plan["bn"] // (128 * plan["cta_group"])
     pk = 1 if plan["cta_group"] == 2 and plan["producer"] != 0 else 0
-    roofline = {"bound": "tensor", "kernel": f"gemm_f16_nt_kernel<{plan['cta_group']},{S},{nw},{pk}>",
+    roofline = {"bound": "tensor",
+                "kernel": f"gemm_f16_nt_kernel<{plan['cta_group']},{S},{nw},{pk},{plan['bk'] // 64}>",
                 "tile": f"{plan['bm']}x{plan['bn']}",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
@@ -750,6 +753,9 @@ def main():
     ap.add_argument("--workload", default="f16_nt_8192", choices=list(inputs.WORKLOADS),
                     help="the seeded workload of the timed GEMM (the s32 one times gemm_s32_nn alone, "
                          "for profiling)")
+    ap.add_argument("--scratch-pool", action="store_true",
+                    help="gemm_set_scratch_pool(1): operands TMA cannot address are repacked into pooled "
+                         "scratch instead of read in place")
     ap.add_argument("--tile", choices=["auto", "narrow"], default="auto",
                     help="narrow: the 256x256 pair tile for every S (GEMM_DEBUG_FORCE_NARROW_TILE), as in "
                          "the same-tile S sweep")
