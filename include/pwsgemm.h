@@ -184,19 +184,23 @@ int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const ge
  * gemm_f16_nt_noalloc -- gemm_f16_nt for callers that cannot allocate device
  * memory.  The pages have no counterpart to this entry point.
  *
- * Same arguments, layouts, results and return codes as gemm_f16_nt.  Where
- * gemm_f16_nt takes scratch from its memory pool (operands whose rows the
- * tensor memory accelerator cannot address), this call uses a fixed 32 MiB
- * array in device memory that exists from the moment the library is loaded
- * until the process exits, on every GPU that loads it.  It never asks the
+ * Same arguments, layouts, results and return codes as gemm_f16_nt.  For
+ * operands whose rows the tensor memory accelerator cannot address,
+ * gemm_f16_nt reads them in place (allocating nothing, but slower for large
+ * operands) or, with gemm_set_scratch_pool(1), repacks them into pooled
+ * scratch.  This call repacks them into a fixed 32 MiB array in device
+ * memory instead: as fast as the pooled repack, with no allocation.  The
+ * array exists from the moment the library is loaded until the process
+ * exits, on every GPU that loads it.  It never asks the
  * driver or any allocator for memory, which suits code running under a
  * fixed device-memory budget, code that has reserved all device memory up
  * front, and code that must not enter an allocator (which may synchronize or
  * fail at a point the caller cannot handle).
  *   - Scratch needed: round256(M*Kp*2) + round256(N*Kp*2) bytes, Kp = K
  *     rounded up to a multiple of 8.  Operands that would need more than the
- *     32 MiB (33554432 bytes) are read in place by the asynchronous-copy
- *     producer instead, which needs no scratch (slower, same result bits).
+ *     32 MiB (33554432 bytes) are read in place by the realigning producer
+ *     instead, as gemm_f16_nt reads them by default (slower for large
+ *     operands, same result bits).
  *     Operands the accelerator can address directly need no scratch at all.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
