@@ -758,3 +758,46 @@ def test_f16_8192_sweep_identical_across_stages():
     # every one of the 67 M outputs against the f64 oracle: 1.1 TFLOP of f64
     # work, about half a minute on 16 host cores
     assert_f16_ok(first.cpu().numpy(), oracle.gemm_f16_nt_f64(a, b), wl.K)
+
+
+def _random_cases(n, seed=2026):
+    rng = np.random.default_rng(seed)
+    flag_sets = [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE, pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE,
+                 pws.GEMM_DEBUG_FORCE_SOLO_TILE, pws.GEMM_DEBUG_FORCE_KSPLIT, pws.GEMM_DEBUG_NO_SPLIT,
+                 pws.GEMM_DEBUG_FORCE_DOUBLE_SLOT, pws.GEMM_DEBUG_FORCE_DIRECT_STORE, POOL]
+    cases = []
+    for _ in range(n):
+        M = int(rng.integers(1, 1300))
+        N = int(rng.integers(1, 1300))
+        K = int(rng.integers(1, 1400))
+        S = int(rng.integers(1, 7))
+        offs = (int(rng.integers(0, 8)), int(rng.integers(0, 8)))
+        flags = flag_sets[int(rng.integers(0, len(flag_sets)))]
+        cases.append((M, N, K, S, offs, flags))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,S,offs,flags", _random_cases(40))
+def test_f16_random_shapes_offsets_and_plans_against_the_oracle(M, N, K, S, offs, flags):
+    # Seeded random shapes, element offsets of each operand from a 16-byte
+    # boundary (0 with K % 8 == 0: TMA; otherwise the realigning producer or,
+    # with the pool, the repack), ring depths and plan switches: every output
+    # against the oracle, and the status word clean.
+    a_np = inputs.normal_f16(M * 7 + K, 0, (M, K))
+    b_np = inputs.normal_f16(N * 5 + K, 1, (N, K))
+    big_a = torch.zeros(M * K + 8, dtype=torch.float16, device="cuda")
+    big_b = torch.zeros(N * K + 8, dtype=torch.float16, device="cuda")
+    a_t = big_a[offs[0]:offs[0] + M * K].view(M, K)
+    b_t = big_b[offs[1]:offs[1] + N * K].view(N, K)
+    a_t.copy_(torch.from_numpy(a_np))
+    b_t.copy_(torch.from_numpy(b_np))
+    pws.gemm_set_debug_flags(flags & ~POOL)
+    pws.gemm_set_scratch_pool(bool(flags & POOL))
+    try:
+        out = pws.gemm_f16_nt(a_t, b_t, stages=S)
+        torch.cuda.synchronize()
+    finally:
+        pws.gemm_set_debug_flags(0)
+        pws.gemm_set_scratch_pool(False)
+    assert pws.gemm_device_status() == pws.GEMM_OK
+    assert_f16_ok(out.cpu().numpy(), oracle.gemm_f16_nt_f64(a_np, b_np), K)
