@@ -447,13 +447,15 @@ def extra_configs(pws, torch, stream):
         a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(name))
         c = torch.empty(wl.M, wl.N, dtype=torch.float16, device=dev)
         # the ragged shape (rows no tensor map describes) is timed on each of
-        # its paths: read in place by the realigning producer (the default:
-        # nothing allocated), repacked into pooled scratch + TMA
-        # (gemm_set_scratch_pool), repacked into the no-alloc call's fixed
-        # array + TMA, and the 4-byte cp.async producer
+        # its paths: repacked into the library's fixed array + TMA (the
+        # default: nothing allocated), read in place by the realigning
+        # producer, repacked into pooled scratch + TMA (gemm_set_scratch_pool),
+        # the no-alloc entry point (fixed array, rows 8-element aligned) and
+        # the 4-byte cp.async producer
         variants = [("", 0, False, pws.gemm_f16_nt)]
         if name.startswith("f16_nt_ragged"):
-            variants += [("pooled_repack", 0, True, pws.gemm_f16_nt),
+            variants += [("in_place", pws.GEMM_DEBUG_IN_PLACE, False, pws.gemm_f16_nt),
+                         ("pooled_repack", 0, True, pws.gemm_f16_nt),
                          ("noalloc", 0, False, pws.gemm_f16_nt_noalloc),
                          ("copy_producer", pws.GEMM_DEBUG_FORCE_COPY_PRODUCER, False, pws.gemm_f16_nt)]
         for suffix, flags, pool, call in variants:
@@ -461,10 +463,9 @@ def extra_configs(pws, torch, stream):
             pws.gemm_set_scratch_pool(pool)
             try:
                 plan = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), wl.stages[0])
-                label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B", 2: "repack+tma",
+                label = {0: "tma", 1: f"cp.async{plan['copy_bytes']}B",
+                         2: "repack into pooled scratch+tma" if pool else "repack into the fixed array+tma",
                          3: "realign in place"}[plan["producer"]]
-                if call is pws.gemm_f16_nt_noalloc:
-                    label = "repack into the fixed array+tma" if plan["producer"] == 3 else label
                 res = {"producer": label, "cta_group": plan["cta_group"]}
                 small = wl.flops < 2 ** 34        # launch-bound: time from a CUDA graph
                 for s in wl.stages:

@@ -130,12 +130,21 @@ int gemm_s32_nn_ring(int64_t M, int64_t N, int64_t K, const int32_t* lhs, const 
  *
  * The producer uses the tensor memory accelerator (TMA) when both operands
  * start on 16-byte boundaries and K is a multiple of 8 (row stride a multiple
- * of 16 bytes).  Otherwise eight producer warps per CTA read the operands in
- * place: each row's K strip is loaded as the aligned 16-byte blocks that hold
- * it, shifted into place in registers and written into the same swizzled ring
- * slot TMA would fill; any tile shape can use it, and nothing is allocated
- * (gemm_set_scratch_pool offers a faster path for large such operands that
- * allocates).  Partial tiles are zero-filled on load and clipped on store.
+ * of 16 bytes).  Otherwise the call first copies both operands into aligned
+ * rows (ceil(K/64)*64 elements apart where that fits, else ceil(K/8)*8) of a
+ * fixed 32 MiB array in device memory that the library holds from load time,
+ * and TMA reads the copy; nothing is allocated.  Every use of that array on a
+ * device is ordered after the previous one with an event (the call's stream
+ * waits, on the GPU, for the previous user's GEMM), so calls on different
+ * streams never overlap on it; such calls serialise with each other.  When
+ * the copy does not fit in the array, or `stream` is being captured into a
+ * CUDA graph (which cannot wait for an event recorded outside it), eight
+ * producer warps per CTA read the operands in place instead: each row's K
+ * strip is loaded as the aligned 16-byte blocks that hold it, shifted into
+ * place in registers and written into the same swizzled ring slot TMA would
+ * fill, on any tile (slower for large operands).  gemm_set_scratch_pool
+ * offers pooled scratch instead of the array.  Every path gives the same
+ * result bits.  Partial tiles are zero-filled on load and clipped on store.
  *
  * Output tiles: 256 x 256 on a CTA pair (two SMs sharing one tcgen05 MMA),
  * or 128 x 128 on one CTA.  The pair tile is used when TMA feeds it and it
@@ -184,33 +193,33 @@ int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const ge
  * gemm_f16_nt_noalloc -- gemm_f16_nt for callers that cannot allocate device
  * memory.  The pages have no counterpart to this entry point.
  *
- * Same arguments, layouts, results and return codes as gemm_f16_nt.  For
- * operands whose rows the tensor memory accelerator cannot address,
- * gemm_f16_nt reads them in place (allocating nothing, but slower for large
- * operands) or, with gemm_set_scratch_pool(1), repacks them into pooled
- * scratch.  This call repacks them into a fixed 32 MiB array in device
- * memory instead: as fast as the pooled repack, with no allocation.  The
- * array exists from the moment the library is loaded until the process
- * exits, on every GPU that loads it.  It never asks the
- * driver or any allocator for memory, which suits code running under a
- * fixed device-memory budget, code that has reserved all device memory up
- * front, and code that must not enter an allocator (which may synchronize or
- * fail at a point the caller cannot handle).
+ * Same arguments, layouts, results and return codes as gemm_f16_nt, and the
+ * same fixed 32 MiB array for operands whose rows the tensor memory
+ * accelerator cannot address, with the same event ordering between its users.
+ * Unlike gemm_f16_nt it never takes pooled scratch, whatever
+ * gemm_set_scratch_pool says, so it never asks the driver or any allocator
+ * for memory: this suits code running under a fixed device-memory budget,
+ * code that has reserved all device memory up front, and code that must not
+ * enter an allocator (which may synchronize or fail at a point the caller
+ * cannot handle).  The array exists from the moment the library is loaded
+ * until the process exits, on every GPU that loads it.
  *   - Scratch needed: round256(M*Kp*2) + round256(N*Kp*2) bytes, Kp = K
  *     rounded up to a multiple of 8.  Operands that would need more than the
  *     32 MiB (33554432 bytes) are read in place by the realigning producer
- *     instead, as gemm_f16_nt reads them by default (slower for large
- *     operands, same result bits).
+ *     instead (slower for large operands, same result bits).
  *     Operands the accelerator can address directly need no scratch at all.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *     The address is kept for the life of the process: after a
  *     cudaDeviceReset (or any other replacement of the device's primary
  *     context) this entry point must not be called again in that process.
- *   - All calls share the one array.  Calls that can overlap on the GPU (on
- *     streams with no ordering between them) race on it: order them.  The
- *     array keeps the last call's contents; each call overwrites every byte
- *     it reads, so nothing needs clearing.
+ *   - All calls share the one array (with gemm_f16_nt).  Outside stream
+ *     capture each use is ordered after the previous one, on the GPU, by an
+ *     event.  A call made while `stream` is being captured into a CUDA graph
+ *     cannot be ordered that way and uses the array unordered: calls that can
+ *     overlap on the GPU then race on it, and the caller must order them.
+ *     The array keeps the last call's contents; each call overwrites every
+ *     byte it reads, so nothing needs clearing.
  */
 int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                         gemm_f16_t* out, int stages, cudaStream_t stream);
@@ -286,6 +295,9 @@ int gemm_set_wait_timeout_ns(uint64_t ns);
  *       64-wide K boxes (three for stages <= 2, two for 3) even when the
  *       tiles exceed one wave.
  *   GEMM_DEBUG_NO_DOUBLE_SLOT      : never use multi-box slots.
+ *   GEMM_DEBUG_IN_PLACE            : read operands that the tensor memory
+ *       accelerator cannot address in place (the realigning producer)
+ *       rather than repacking them.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for unknown bits.
  */
 enum {
@@ -302,7 +314,8 @@ enum {
     GEMM_DEBUG_FORCE_KSPLIT = 1024u,
     GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048u,
     GEMM_DEBUG_FORCE_DOUBLE_SLOT = 4096u,
-    GEMM_DEBUG_NO_DOUBLE_SLOT = 8192u
+    GEMM_DEBUG_NO_DOUBLE_SLOT = 8192u,
+    GEMM_DEBUG_IN_PLACE = 16384u
 };
 int gemm_set_debug_flags(unsigned flags);
 
@@ -310,20 +323,17 @@ int gemm_set_debug_flags(unsigned flags);
  * gemm_set_scratch_pool -- whether later gemm_f16_nt calls may allocate
  * scratch memory (host state only; default 0 = never).
  *
- * Off (the default), operands that the tensor memory accelerator cannot
- * address (rows not a multiple of 16 bytes apart, or a base not 16-byte
- * aligned) are read in place by the realigning producer, and no call
- * allocates device memory.  On, such operands are first copied into rows of
- * ceil(K/64)*64 elements in scratch memory taken stream-ordered from a
- * memory pool the library owns on the current device (about
- * (M+N)*ceil(K/64)*128 bytes per call, returned to the pool on `stream`
- * after the GEMM; the pool keeps freed memory, so repeated calls of one size
- * request no new memory from the driver), and the copy is read with TMA.
- * That copy pays for itself on large operands: measured on GB300 at
- * 4000 x 3000 x 2050, S = 3, the call takes 49 us with the pool and 140 us
+ * On, operands that the tensor memory accelerator cannot address are copied
+ * into rows of ceil(K/64)*64 elements in scratch memory taken stream-ordered
+ * from a memory pool the library owns on the current device (about
+ * (M+N)*ceil(K/64)*128 bytes per call, returned to the pool on `stream` after
+ * the GEMM; the pool keeps freed memory, so repeated calls of one size request
+ * no new memory from the driver), instead of into the library's fixed array.
+ * Each call then has its own copy, so such calls on different streams can
+ * overlap, and operands too large for the array are repacked rather than read
  * in place.  If the pool cannot supply the scratch, the call reads the
- * operands in place after all.  Results are bitwise identical either way.
- * Returns GEMM_OK.
+ * operands in place.  Results are bitwise identical either way.
+ * gemm_f16_nt_noalloc ignores this setting.  Returns GEMM_OK.
  */
 int gemm_set_scratch_pool(int enable);
 
@@ -335,8 +345,10 @@ int gemm_set_scratch_pool(int enable);
  *   plan[2] K per ring slot (64; 192 or 128 for multi-box slots)
  *   plan[3] CTAs per tile (1 or 2)
  *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy,
- *           2 = tensor memory accelerator on an aligned scratch copy
- *           (gemm_set_scratch_pool), 3 = realigning loads in place
+ *           2 = tensor memory accelerator on an aligned copy (in the fixed
+ *           array, or in pooled scratch with gemm_set_scratch_pool; a call on
+ *           a stream being captured reads in place instead), 3 = realigning
+ *           loads in place
  *   plan[5] copy granularity in bytes (16 for TMA, else 8, 4 or 2)
  *   plan[6] output store: 0 = tensor memory accelerator, 1 = plain stores
  *   plan[7] dynamic shared memory bytes per CTA

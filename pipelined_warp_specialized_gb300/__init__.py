@@ -43,6 +43,7 @@ GEMM_DEBUG_FORCE_KSPLIT = 1024
 GEMM_DEBUG_SKIP_KSPLIT_SEND = 2048
 GEMM_DEBUG_FORCE_DOUBLE_SLOT = 4096
 GEMM_DEBUG_NO_DOUBLE_SLOT = 8192
+GEMM_DEBUG_IN_PLACE = 16384
 
 _lib = None
 

@@ -1712,6 +1712,10 @@ int launch_plan(int stages, const Plan& pl, const DeviceInfo& info, const CUtens
                       : launch_stages<2, 1, 0>(stages, pl, info, ta, tb, tbh, tc, p, stream);
 }
 
+// Whether gemm_f16_nt repacks operands TMA cannot address (defined with the
+// fixed scratch array below).
+bool wants_repack(int64_t M, int64_t N, int64_t K, unsigned flags);
+
 }  // namespace f16nt
 }  // namespace pws
 
@@ -1723,7 +1727,7 @@ extern "C" int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_
     if (!plan) return GEMM_ERR_INVALID_ARG;
     const unsigned flags = pws::debug_flags();
     const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, pws::sm_count_or_default(), flags,
-                              pws::scratch_pool_enabled());
+                              wants_repack(M, N, K, flags));
     plan[0] = 128 * pl.cg;
     plan[1] = 128 * pl.cg * pl.nw;
     plan[2] = BK * pl.kb;
@@ -1821,6 +1825,122 @@ int run_plan(const Plan& pl, const DeviceInfo& info, int64_t M, int64_t N, int64
 }  // namespace f16nt
 }  // namespace pws
 
+// ---------------------------------------------------------------- the library's fixed scratch array
+//
+// Operands whose rows the tensor memory accelerator cannot address are
+// fastest copied once into aligned rows and read by TMA (the in-place
+// producer realigns every K block of every tile it reads).  The copy needs
+// scratch memory, and no call may allocate: so it goes to a fixed array in
+// device memory that exists from the moment the library is loaded.  Every
+// GPU that loads the library holds it until the process exits.
+//
+// Every use of the array on a device is ordered after the previous one: the
+// call's stream waits for an event recorded after the previous user's GEMM,
+// on whatever stream that was, and records it again after its own.  Calls on
+// different streams therefore serialise on the GPU where they share the
+// array, without any host synchronisation.  A stream being captured into a
+// CUDA graph cannot wait for an event recorded outside the capture, so
+// gemm_f16_nt reads the operands in place there, and gemm_f16_nt_noalloc uses
+// the array unordered (its caller orders such calls).
+namespace pws {
+namespace f16nt {
+
+constexpr size_t kFixedScratchBytes = static_cast<size_t>(32) << 20;   // 32 MiB
+
+// The scratch array.  In host code its name only stands in for the symbol:
+// it is not a device address, and passing it to a kernel would fault (or,
+// where the GPU can reach host memory, silently use the wrong memory).  The
+// device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+struct FixedScratch {
+    std::mutex mu;                  // per-device state, and "wait; launch; record" as one step
+    void* addr[64] = {};
+    cudaEvent_t done[64] = {};      // recorded after the last user's GEMM
+    bool used[64] = {};
+};
+FixedScratch g_fixed;
+
+bool stream_capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return true;                // unknown: take the path that needs no ordering
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
+// Runs body(array address) for a call on `stream`; with `ordered`, after the
+// previous user of the array and before the next.  The first use on a device
+// looks up the address and creates the event.
+template <class F>
+int with_fixed_scratch(int device, cudaStream_t stream, bool ordered, F&& body) {
+    if (device < 0 || device >= 64) return GEMM_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lk(g_fixed.mu);
+    if (!g_fixed.addr[device]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fixed_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        g_fixed.addr[device] = p;
+    }
+    if (ordered) {
+        if (!g_fixed.done[device] &&
+            cudaEventCreateWithFlags(&g_fixed.done[device], cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            g_fixed.done[device] = nullptr;
+            return GEMM_ERR_LAUNCH;
+        }
+        if (g_fixed.used[device] && cudaStreamWaitEvent(stream, g_fixed.done[device], 0) != cudaSuccess)
+            return GEMM_ERR_LAUNCH;
+    }
+    const int rc = body(g_fixed.addr[device]);
+    if (ordered) {
+        // recorded even after a failed launch: the stream's earlier work
+        // still orders the next user correctly
+        if (cudaEventRecord(g_fixed.done[device], stream) != cudaSuccess) return GEMM_ERR_LAUNCH;
+        g_fixed.used[device] = true;
+    }
+    return rc;
+}
+
+// Repacks both operands into the array (rows `row_align` elements apart) and
+// runs the TMA plan on the copy.
+int run_repacked_in_array(void* scratch, const DeviceInfo& info, int64_t M, int64_t N, int64_t K, const void* lhs,
+                          const void* rhs, void* out, int stages, unsigned flags, int64_t row_align,
+                          cudaStream_t stream) {
+    size_t b_off = 0;
+    repack_bytes(M, N, K, &b_off, row_align);
+    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, true);
+    // The repack writes every scratch byte the GEMM then reads (rows up to
+    // ceil(K/8)*8 elements, the rest of a longer row is never read), so
+    // nothing left over from an earlier call is ever used.
+    const int64_t Kw = repack_ld(K, 8), Kp = repack_ld(K, row_align);
+    uint16_t* da = static_cast<uint16_t*>(scratch);
+    uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
+    if (launch_repack(lhs, M, rhs, N, K, Kw, Kp, da, db, stream) != cudaSuccess) return GEMM_ERR_LAUNCH;
+    return run_plan(pl, info, M, N, K, lhs, rhs, out, da, db, Kp, stages, flags, stream);
+}
+
+// Row alignment (elements) of a repack into the array: 64 (128-byte rows,
+// which TMA reads fastest) when that fits, else 8, else 0 (does not fit).
+int64_t fixed_row_align(int64_t M, int64_t N, int64_t K) {
+    if (repack_bytes(M, N, K, nullptr, kPooledRowAlign) <= kFixedScratchBytes) return kPooledRowAlign;
+    if (repack_bytes(M, N, K, nullptr, 8) <= kFixedScratchBytes) return 8;
+    return 0;
+}
+
+// Whether gemm_f16_nt repacks operands TMA cannot address (pooled scratch,
+// or the fixed array where they fit), rather than reading them in place.
+bool wants_repack(int64_t M, int64_t N, int64_t K, unsigned flags) {
+    if (flags & GEMM_DEBUG_IN_PLACE) return false;
+    return scratch_pool_enabled() || fixed_row_align(M, N, K) > 0;
+}
+
+}  // namespace f16nt
+}  // namespace pws
+
 extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                            gemm_f16_t* out, int stages, cudaStream_t stream) {
     using namespace pws;
@@ -1833,12 +1953,21 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
     if (rc != GEMM_OK) return rc;
     if (K == 0) return zero_output(out, M, N, info, stream);
     const unsigned flags = debug_flags();
-    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, scratch_pool_enabled());
+    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, wants_repack(M, N, K, flags));
 
-    // Operands whose rows TMA cannot address are read in place by the
-    // realigning producer.  With gemm_set_scratch_pool(1) they are copied to
-    // aligned rows in pooled scratch memory first and read by TMA (if the
-    // pool cannot supply it, they are read in place after all).
+    // Operands whose rows TMA cannot address are copied to aligned rows and
+    // read by TMA: into pooled scratch with gemm_set_scratch_pool(1), else
+    // into the library's fixed array where they fit (ordered after its
+    // previous user).  Otherwise -- too large, a stream being captured, the
+    // pool out of memory -- the realigning producer reads them in place.
+    if (pl.repack && !scratch_pool_enabled()) {
+        const int64_t align = fixed_row_align(M, N, K);
+        if (align > 0 && !stream_capturing(stream))
+            return with_fixed_scratch(info.device, stream, true, [&](void* scratch) {
+                return run_repacked_in_array(scratch, info, M, N, K, lhs, rhs, out, stages, flags, align, stream);
+            });
+        pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
+    }
     const void* a_src = lhs;
     const void* b_src = rhs;
     int64_t ld = K;
@@ -1869,50 +1998,14 @@ extern "C" int gemm_f16_nt(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lh
 
 // ---------------------------------------------------------------- no-allocation variant
 //
-// gemm_f16_nt gets the scratch of its repack step (operands whose rows the
-// tensor memory accelerator cannot address) from a memory pool, which may
-// have to ask the driver for memory.  Some callers cannot allow that: code
-// running under a fixed device-memory budget that must not grow, code that
-// must not call into the allocator at all (it can synchronise or fail at a
-// point the caller cannot handle), or code that has reserved all device
-// memory up front.  gemm_f16_nt_noalloc serves them with scratch that exists
-// from the moment the library is loaded: a fixed array in device memory.
-// Operands that would need more scratch than the array holds are read in
-// place by the cp.async producer, which needs none.
-namespace pws {
-namespace f16nt {
-
-constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;   // 32 MiB
-
-// The scratch array.  Every GPU that loads this library holds it until the
-// process exits.  In host code its name only stands in for the symbol: it is
-// not a device address, and passing it to a kernel would fault (or, where the
-// GPU can reach host memory, silently use the wrong memory).  The device
-// address comes from cudaGetSymbolAddress, once per device.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
-
-// Device address of the scratch array on `device` (the current device).
-// The first call per device looks it up; returns nullptr on failure.
-void* noalloc_scratch(int device) {
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (device < 0 || device >= 64) return nullptr;
-    if (!g_noalloc_addr[device]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        g_noalloc_addr[device] = p;
-    }
-    return g_noalloc_addr[device];
-}
-
-}  // namespace f16nt
-}  // namespace pws
-
+// gemm_f16_nt_noalloc is gemm_f16_nt for callers that cannot allocate device
+// memory: code running under a fixed device-memory budget that must not
+// grow, code that must not call into the allocator at all (it can
+// synchronise or fail at a point the caller cannot handle), or code that has
+// reserved all device memory up front.  It never takes pooled scratch,
+// whatever gemm_set_scratch_pool says: operands TMA cannot address go to the
+// fixed array (rows ceil(K/8)*8 elements apart, the documented limit) or,
+// when they do not fit, are read in place.
 extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                                    gemm_f16_t* out, int stages, cudaStream_t stream) {
     using namespace pws;
@@ -1925,30 +2018,11 @@ extern "C" int gemm_f16_nt_noalloc(int64_t M, int64_t N, int64_t K, const gemm_f
     if (rc != GEMM_OK) return rc;
     if (K == 0) return zero_output(out, M, N, info, stream);
     const unsigned flags = debug_flags();
-    Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags, true);
-
-    const void* a_src = lhs;
-    const void* b_src = rhs;
-    int64_t ld = K;
-    if (pl.repack) {
-        size_t b_off = 0;
-        if (repack_bytes(M, N, K, &b_off, 8) > kNoAllocScratchBytes) {
-            // more scratch than the array holds: the producer that reads the
-            // operands in place needs none
-            pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags);
-        } else {
-            void* scratch = noalloc_scratch(info.device);
-            if (!scratch) return GEMM_ERR_LAUNCH;
-            // The repack writes every scratch byte the GEMM then reads (padding
-            // included), so nothing left over from an earlier call is ever used.
-            const int64_t Kp = (K + 7) / 8 * 8;
-            uint16_t* da = static_cast<uint16_t*>(scratch);
-            uint16_t* db = reinterpret_cast<uint16_t*>(static_cast<char*>(scratch) + b_off);
-            if (launch_repack(lhs, M, rhs, N, K, Kp, Kp, da, db, stream) != cudaSuccess) return GEMM_ERR_LAUNCH;
-            a_src = da;
-            b_src = db;
-            ld = Kp;
-        }
-    }
-    return run_plan(pl, info, M, N, K, lhs, rhs, out, a_src, b_src, ld, stages, flags, stream);
+    const bool fits = repack_bytes(M, N, K, nullptr, 8) <= kFixedScratchBytes;
+    const Plan pl = make_plan(M, N, K, lhs, rhs, out, stages, info.num_sms, flags,
+                              fits && !(flags & GEMM_DEBUG_IN_PLACE));
+    if (!pl.repack) return run_plan(pl, info, M, N, K, lhs, rhs, out, lhs, rhs, K, stages, flags, stream);
+    return with_fixed_scratch(info.device, stream, !stream_capturing(stream), [&](void* scratch) {
+        return run_repacked_in_array(scratch, info, M, N, K, lhs, rhs, out, stages, flags, 8, stream);
+    });
 }

@@ -230,7 +230,7 @@ int gemm_set_debug_flags(unsigned flags) {
                            GEMM_DEBUG_FORCE_NARROW_TILE | GEMM_DEBUG_FORCE_WIDE_TILE |
                            GEMM_DEBUG_SKIP_ACC_SEED | GEMM_DEBUG_NO_KSPLIT | GEMM_DEBUG_FORCE_KSPLIT |
                            GEMM_DEBUG_SKIP_KSPLIT_SEND | GEMM_DEBUG_FORCE_DOUBLE_SLOT |
-                           GEMM_DEBUG_NO_DOUBLE_SLOT;
+                           GEMM_DEBUG_NO_DOUBLE_SLOT | GEMM_DEBUG_IN_PLACE;
     if (flags & ~known) return GEMM_ERR_INVALID_ARG;
     pws::g_flags.store(flags, std::memory_order_relaxed);
     return GEMM_OK;

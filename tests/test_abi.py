@@ -123,7 +123,7 @@ def test_s32_ring_argument_checks_return_before_launch(lib, args, want):
 
 
 def test_debug_flags_and_timeout_setters(lib):
-    assert lib.gemm_set_debug_flags(1 << 14) == pws.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_set_debug_flags(1 << 15) == pws.GEMM_ERR_INVALID_ARG
     assert lib.gemm_set_debug_flags(0) == pws.GEMM_OK
     assert lib.gemm_set_wait_timeout_ns(0) == pws.GEMM_OK
 
@@ -257,22 +257,31 @@ def test_plan_k_split_rule(lib):
 
 def test_plan_ragged_shape(lib):
     # K = 2050: rows of 4100 bytes are not 16-byte aligned, so no TMA descriptor
-    # exists for the operands as given: the realigning producer reads them in
-    # place (nothing is allocated), on the same tile TMA would get
+    # exists for the operands as given.  They fit the library's fixed 32 MiB
+    # array in 128-byte rows (7000 x 2112 x 2 bytes): repacked there, then fed
+    # by TMA; nothing is allocated
     p = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
-    assert p["producer"] == 3 and p["copy_bytes"] == 16
+    assert p["producer"] == 2 and p["copy_bytes"] == 16
     assert p["cta_group"] == 2 and p["bm"] == 256               # 16 x 12 pair tiles >= 152 / 2
     assert p["bn"] == 512                       # N = 3000: 6 wide tile columns pad no more than 12 narrow ones
     assert p["store"] == 0                      # 6000-byte output rows are 16-byte aligned
     assert p["tiles"] == 16 * 6 and p["k_blocks"] == 33
-    # with the scratch pool allowed they are repacked, then fed by TMA: same tile
-    pws.gemm_set_scratch_pool(True)
+    # read in place by the realigning producer: the same tile
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_IN_PLACE)
     try:
         r = pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)
     finally:
+        pws.gemm_set_debug_flags(0)
+    assert r["producer"] == 3 and {k: r[k] for k in ("bm", "bn", "tiles")} == {k: p[k] for k in ("bm", "bn", "tiles")}
+    # too large for the array (16384 rows of 2112 elements): read in place,
+    # unless the scratch pool is allowed
+    assert pws.gemm_f16_nt_plan(8192, 8192, 2050, stages=3)["producer"] == 3
+    pws.gemm_set_scratch_pool(True)
+    try:
+        assert pws.gemm_f16_nt_plan(8192, 8192, 2050, stages=3)["producer"] == 2
+    finally:
         pws.gemm_set_scratch_pool(False)
-    assert r["producer"] == 2 and {k: r[k] for k in ("bm", "bn", "tiles")} == {k: p[k] for k in ("bm", "bn", "tiles")}
-    assert pws.gemm_f16_nt_plan(4000, 3000, 2050, stages=3)["producer"] == 3      # the setter is host state
+    assert pws.gemm_f16_nt_plan(8192, 8192, 2050, stages=3)["producer"] == 3      # the setter is host state
     # the async-copy producer reads them in place (single-CTA tile, 4-byte copies)
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
     try:
@@ -299,9 +308,16 @@ def test_plan_rejects_tile_counts_beyond_int(lib):
 
 
 def test_plan_edge_cases(lib):
-    assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 3            # odd K: read in place
+    assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 2            # odd K: repacked into the fixed array
     assert pws.gemm_f16_nt_plan(7, 9, 3)["store"] == 1               # odd N: plain stores
-    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 3   # unaligned base
+    assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 2   # unaligned base
+    pws.gemm_set_debug_flags(pws.GEMM_DEBUG_IN_PLACE)
+    try:
+        assert pws.gemm_f16_nt_plan(7, 9, 3)["producer"] == 3
+        assert pws.gemm_f16_nt_plan(64, 64, 16, lhs_ptr=A + 2)["producer"] == 3
+        assert pws.gemm_f16_nt_plan(64, 64, 16)["producer"] == 0      # aligned: TMA either way
+    finally:
+        pws.gemm_set_debug_flags(0)
     assert pws.gemm_f16_nt_plan(64, 64, 16)["producer"] == 0
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)
     try:
@@ -317,7 +333,7 @@ def test_plan_edge_cases(lib):
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE)
     try:
         assert pws.gemm_f16_nt_plan(300, 300, 64)["cta_group"] == 2
-        assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 2   # read in place on the pair tile
+        assert pws.gemm_f16_nt_plan(300, 300, 66)["cta_group"] == 2   # repacked, or read in place, on the pair tile
     finally:
         pws.gemm_set_debug_flags(0)
     pws.gemm_set_debug_flags(pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_COPY_PRODUCER)

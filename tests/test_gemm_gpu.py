@@ -374,11 +374,12 @@ def test_f16_k_zero_and_empty():
     assert out.shape == (0, 4)
 
 
-@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_FORCE_PAIR_TILE,
-                                   pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE,
-                                   pws.GEMM_DEBUG_FORCE_KSPLIT, POOL,
+@pytest.mark.parametrize("flags", [0, pws.GEMM_DEBUG_IN_PLACE, pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_PAIR_TILE,
+                                   pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE,
+                                   pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_KSPLIT, POOL,
                                    pws.GEMM_DEBUG_FORCE_COPY_PRODUCER],
-                         ids=["realign", "realign_pair", "realign_wide", "realign_ksplit", "repack", "copy"])
+                         ids=["fixed_array", "realign", "realign_pair", "realign_wide", "realign_ksplit", "pooled",
+                              "copy"])
 def test_f16_unaligned_operands(flags):
     M, N, K = 150, 90, 128
     big_a = _dev(inputs.uniform_f16(5, 0, (M * K + 1,)))
@@ -404,18 +405,21 @@ def test_f16_unaligned_every_row_alignment(offset):
     # consecutive rows start 2 bytes further on, so every even byte offset
     # 0..14 occurs as a row start, for both operands, and the last rows end
     # near the buffers' ends.  In place on the single-CTA, pair and wide
-    # tiles; repacked into pooled scratch and into the no-alloc array.
+    # tiles; repacked into the fixed array (gemm_f16_nt's default and the
+    # no-alloc call) and into pooled scratch.
     M, N, K = 37, 45, 1027
     big_a = _dev(inputs.normal_f16(60 + offset, 0, (M * K + 8,)))
     big_b = _dev(inputs.normal_f16(60 + offset, 1, (N * K + 8,)))
     a_t = big_a[offset:offset + M * K].view(M, K)
     b_t = big_b[7 - offset:7 - offset + N * K].view(N, K)
-    assert pws.gemm_f16_nt_plan(M, N, K, a_t.data_ptr(), b_t.data_ptr(), 3 << 40)["producer"] == 3
+    assert pws.gemm_f16_nt_plan(M, N, K, a_t.data_ptr(), b_t.data_ptr(), 3 << 40)["producer"] == 2
     ref = oracle.gemm_f16_nt_f64(a_t.cpu().numpy(), b_t.cpu().numpy())
     outs = []
-    for fn, flags in ((pws.gemm_f16_nt, 0), (pws.gemm_f16_nt, pws.GEMM_DEBUG_FORCE_PAIR_TILE),
-                      (pws.gemm_f16_nt, pws.GEMM_DEBUG_FORCE_PAIR_TILE | pws.GEMM_DEBUG_FORCE_WIDE_TILE),
-                      (pws.gemm_f16_nt, POOL), (pws.gemm_f16_nt_noalloc, 0)):
+    for fn, flags in ((pws.gemm_f16_nt, pws.GEMM_DEBUG_IN_PLACE),
+                      (pws.gemm_f16_nt, pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_PAIR_TILE),
+                      (pws.gemm_f16_nt, pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_PAIR_TILE |
+                       pws.GEMM_DEBUG_FORCE_WIDE_TILE),
+                      (pws.gemm_f16_nt, 0), (pws.gemm_f16_nt, POOL), (pws.gemm_f16_nt_noalloc, 0)):
         pws.gemm_set_debug_flags(flags & ~POOL)
         pws.gemm_set_scratch_pool(bool(flags & POOL))
         try:
@@ -477,6 +481,7 @@ def test_f16_realign_equals_tma_bitwise(M, N, K, S, flags, want):
     a_u.copy_(torch.from_numpy(a_np))
     b_u.copy_(torch.from_numpy(b_np))
     a_al, b_al = _dev(a_np), _dev(b_np)
+    flags |= pws.GEMM_DEBUG_IN_PLACE           # the unaligned operands are read in place
     pws.gemm_set_debug_flags(flags)
     try:
         p_u = pws.gemm_f16_nt_plan(M, N, K, a_u.data_ptr(), b_u.data_ptr(), 3 << 40, S)
@@ -553,18 +558,20 @@ def test_f16_4096_config_full():
 
 def test_f16_ragged_config_full():
     # K = 2050: rows of 4100 bytes, which no tensor map describes.  The
-    # default path reads them in place with the realigning producer on the
-    # wide pair tile; also on the 256 x 256 pair and the single-CTA tiles, the
-    # pooled repack + TMA and the async-copy producer.  All against the
-    # oracle, and the tiles bitwise equal to each other.
+    # default path repacks them into the library's fixed array and runs the
+    # wide pair tile on the copy; also read in place by the realigning
+    # producer on the wide, 256 x 256 pair and single-CTA tiles, the pooled
+    # repack and the async-copy producer.  All against the oracle, and the
+    # tiles bitwise equal to each other.
     wl = inputs.WORKLOADS["f16_nt_ragged_4000x3000x2050"]
     a, b = wl.lhs(), wl.rhs()
     p = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, stages=3)
-    assert (p["producer"], p["cta_group"], p["bn"]) == (3, 2, 512)
+    assert (p["producer"], p["cta_group"], p["bn"]) == (2, 2, 512)
     ref = oracle.gemm_f16_nt_f64(a, b)
     outs = []
-    for flags in (0, pws.GEMM_DEBUG_FORCE_NARROW_TILE, pws.GEMM_DEBUG_FORCE_SOLO_TILE,
-                  POOL, pws.GEMM_DEBUG_FORCE_COPY_PRODUCER):
+    for flags in (0, pws.GEMM_DEBUG_IN_PLACE, pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_NARROW_TILE,
+                  pws.GEMM_DEBUG_IN_PLACE | pws.GEMM_DEBUG_FORCE_SOLO_TILE, POOL,
+                  pws.GEMM_DEBUG_FORCE_COPY_PRODUCER):
         got = run_f16(a, b, 3, flags)
         assert_f16_ok(got, ref, wl.K)
         outs.append(got.view(np.uint16))
@@ -596,6 +603,63 @@ def test_f16_repack_scratch_is_stream_ordered():
         assert pws.gemm_device_status() == pws.GEMM_OK
         for (a, b, da, db, ref), o in zip(cases, outs):
             assert_f16_ok(o.cpu().numpy(), ref, K)
+
+
+def test_f16_fixed_array_shared_by_calls_on_four_streams():
+    # Unaligned-K GEMMs on four streams, each repacked into the library's one
+    # fixed array: every use is ordered after the previous one by an event,
+    # so no call reads another's copy.  Rounds with different inputs, each
+    # output against the oracle; also through the no-alloc entry point.
+    M, N, K = 520, 640, 1030
+    cases = []
+    for seed in range(43, 47):
+        a = inputs.uniform_f16(seed, 0, (M, K))
+        b = inputs.uniform_f16(seed, 1, (N, K))
+        cases.append((_dev(a), _dev(b), oracle.gemm_f16_nt_f64(a, b)))
+    assert pws.gemm_f16_nt_plan(M, N, K)["producer"] == 2
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    outs = [torch.empty(M, N, dtype=torch.float16, device="cuda") for _ in range(4)]
+    torch.cuda.synchronize()
+    for fn in (pws.gemm_f16_nt, pws.gemm_f16_nt_noalloc, pws.gemm_f16_nt):
+        for r in range(3):
+            for i, (st, o) in enumerate(zip(streams, outs)):
+                da, db, _ = cases[(i + r) % 4]
+                fn(da, db, o, stages=3, stream=st)
+            torch.cuda.synchronize()
+            for s_ in streams:
+                assert pws.gemm_device_status(s_) == pws.GEMM_OK
+            for i, o in enumerate(outs):
+                assert_f16_ok(o.cpu().numpy(), cases[(i + r) % 4][2], K)
+
+
+def test_f16_unaligned_calls_inside_graph_capture():
+    # A stream being captured cannot wait for the fixed array's event, so
+    # gemm_f16_nt reads unaligned operands in place there (the no-alloc call
+    # uses the array, unordered); the replayed graph gives the same bits as
+    # the eager calls, which repack into the array.
+    M, N, K = 300, 260, 1030
+    a_np = inputs.normal_f16(48, 0, (M, K))
+    b_np = inputs.normal_f16(48, 1, (N, K))
+    a, b = _dev(a_np), _dev(b_np)
+    ref = oracle.gemm_f16_nt_f64(a_np, b_np)
+    eager = pws.gemm_f16_nt(a, b, stages=2)
+    torch.cuda.synchronize()
+    for fn in (pws.gemm_f16_nt, pws.gemm_f16_nt_noalloc):
+        out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn(a, b, out, stages=2, stream=s)          # first call of the process on this path: set-up
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn(a, b, out, stages=2, stream=s)
+        out.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert pws.gemm_device_status(s) == pws.GEMM_OK
+        assert_f16_ok(out.cpu().numpy(), ref, K)
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), eager.cpu().numpy().view(np.uint16))
 
 
 def test_concurrent_gemms_on_four_streams():

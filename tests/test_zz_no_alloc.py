@@ -1,8 +1,8 @@
 """gemm_f16_nt_noalloc, the entry point for callers that cannot allocate
 device memory (a fixed memory budget, memory reserved up front, or code that
-must not enter an allocator).  It runs the same GEMM as gemm_f16_nt but takes
-the scratch of the repack step from a fixed device array loaded with the
-library instead of a memory pool; operands that would need more than the
+must not enter an allocator).  It runs the same GEMM as gemm_f16_nt and
+repacks operands TMA cannot address into the library's fixed device array,
+whatever the scratch-pool setting; operands that would need more than the
 array holds are read in place.  Results are checked against the oracle and
 must equal gemm_f16_nt's bit for bit.
 
@@ -45,7 +45,7 @@ def _bits(t):
 @pytest.mark.parametrize("M,N,K,S,want", [
     # K = 1030: rows of 2060 bytes, which no tensor map describes: this call
     # repacks them into the array (1700 rows x 1032 x 2 bytes, well under
-    # its 32 MiB), while gemm_f16_nt reads them in place
+    # its 32 MiB), as gemm_f16_nt does (in 128-byte rows)
     (1000, 700, 1030, 3, {}),
     # the ragged workload: 7000 rows of 2056 elements, 28.7 MB of the array
     (4000, 3000, 2050, 3, {}),
@@ -54,7 +54,7 @@ def _bits(t):
 ], ids=["1000x700x1030", "ragged_4000x3000x2050", "k_split_300x260x2050"])
 def test_noalloc_matches_the_oracle_on_two_calls_in_a_row(M, N, K, S, want):
     plan = pws.gemm_f16_nt_plan(M, N, K, stages=S)
-    assert plan["producer"] == 3 and {k: plan[k] for k in want} == want, plan
+    assert plan["producer"] == 2 and {k: plan[k] for k in want} == want, plan
     for seed in (71, 72):                       # two calls in a row share the array
         a_np, b_np = _pair(seed, M, N, K)
         a, b = torch.from_numpy(a_np).cuda(), torch.from_numpy(b_np).cuda()
