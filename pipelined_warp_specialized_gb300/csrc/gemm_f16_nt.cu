@@ -16,11 +16,13 @@
 //   * producer  -- one warp (one elected thread) issues the TMA copies:
 //                  wait empty[s], arm full[s] with the byte count, copy A and
 //                  B strips into slot s.  Where TMA cannot address the
-//                  operands (rows not 16-byte aligned), eight warps fill the
-//                  same swizzled layout with cp.async and arrive on full[s]
-//                  once their copies have landed and been fenced to the async
-//                  proxy (CUDA tutorial ch.4, section 4.8.1), S - 1 slots late
-//                  so that S - 1 slots of copies stay in flight.
+//                  operands (rows not 16-byte aligned), the host first
+//                  copies them to aligned rows (the library's fixed array or
+//                  pooled scratch); where that is not possible, eight warps
+//                  fill the same swizzled layout themselves -- aligned
+//                  16-byte loads shifted into place in registers -- and
+//                  arrive on full[s] once their stores have been fenced to
+//                  the async proxy (CUDA tutorial ch.4, section 4.8.1).
 //   * consumer  -- one warp (one elected thread) seeds every empty[s] once
 //                  before its loop ("foreach {s} in [MATMUL_STAGES] trigger
 //                  empty[s]"), then per K block waits full[s], issues four
@@ -100,7 +102,7 @@ static_assert(EPI_WARPS_WIDE * EPI_BUF == EPI_BYTES, "both epilogue forms use th
 template <int NW, int PK>
 constexpr int epi_warps() { return NW == 2 && PK == 0 ? EPI_WARPS_WIDE : EPI_WARPS; }
 constexpr int MAX_STAGES = 6;
-constexpr int COPY_WARPS = 8;          // producer warps of the cp.async producer
+constexpr int COPY_WARPS = 8;          // producer warps of the realigning and cp.async producers
 constexpr int COPY_THREADS = COPY_WARPS * 32;
 #ifndef PWS_GROUP_M
 #define PWS_GROUP_M 8
@@ -1399,7 +1401,8 @@ struct Plan {
 // Fewest K blocks for which small single-CTA GEMMs split K over two CTAs.
 constexpr int kKSplitMinBlocks = 32;
 
-// Row alignment (elements) of the repack copy in pooled scratch.
+// Row alignment (elements) of a repacked copy: 64 elements, 128-byte rows,
+// which TMA reads fastest (the fixed array falls back to 8 when 64 does not fit).
 constexpr int64_t kPooledRowAlign = 64;
 
 // The wide tile's 48 KB slots fit the shared memory up to this many stages.
