@@ -425,9 +425,11 @@ def s32_roofline(torch, stream, us, ops, grid_blocks=128, threads=256):
 
 
 def extra_configs(pws, torch, stream):
-    """Kernel-only timings of every workload (inputs resident)."""
+    """Kernel-only timings of every workload (inputs resident); f16 entries
+    carry their fraction of the measured burst dense 16-bit peak."""
     out = {}
     dev = torch.device("cuda")
+    burst = measured_peaks()[0]["bf16_tflops"]
     wl = inputs.WORKLOADS["s32_nn_128x256x256"]
     a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(wl.name))
     c = torch.empty(wl.M, wl.N, dtype=torch.int32, device=dev)
@@ -475,6 +477,7 @@ def extra_configs(pws, torch, stream):
                         ms = time_steady(lambda: call(a, b, c, stages=s, stream=stream), torch, stream)
                     ps = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), s)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
+                                    "frac_of_burst_peak": round(wl.flops / ms / 1e9 / burst, 4),
                                     "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1),
                                     "tile": f"{ps['bm']}x{ps['bn']}"}
                     res[f"S{s}"]["timing"] = ("CUDA-graph replay"
@@ -498,6 +501,7 @@ def extra_configs(pws, torch, stream):
                 for s in range(1, 7):
                     ms = time_steady(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), torch, stream)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
+                                    "frac_of_burst_peak": round(wl.flops / ms / 1e9 / burst, 4),
                                     "tile": "256x256",
                                     "timing": "0.25 s warm-up, then 0.25 s of back-to-back launches"}
                 plan_n = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), 6)
