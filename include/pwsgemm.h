@@ -56,6 +56,14 @@
 extern "C" {
 #endif
 
+/* The library is built with hidden visibility: the functions declared here
+ * are its only exported symbols.  Its per-process state (tensor-map caches,
+ * per-kernel shared-memory settings) therefore stays private to one copy of
+ * the library even when several copies are loaded into the same process. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 /* Status codes returned by every entry point. */
 typedef enum {
     GEMM_OK = 0,
@@ -359,6 +367,10 @@ int gemm_set_scratch_pool(int enable);
  */
 int gemm_f16_nt_plan(int64_t M, int64_t N, int64_t K, const gemm_f16_t* lhs, const gemm_f16_t* rhs,
                      const gemm_f16_t* out, int stages, int64_t* plan);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
 
 #ifdef __cplusplus
 }

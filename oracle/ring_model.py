@@ -19,6 +19,14 @@ pages state about them:
   the s32 kernel -- a prologue load of tile 0, steady iterations that load
   tile t while computing tile t-1 and then swap the buffer names, and an
   epilogue that computes the last tile.
+* The same chapter's rotate over S buffers, with asynchronous copies: as the
+  TileLang tutorial ch.22 section 4.3 notes, a block barrier does not wait
+  for them, so a tile may be read only after the copy group holding it has
+  been waited for and a barrier has followed, and a buffer may be refilled
+  only after a barrier has followed every read of its previous tile.
+  ``ring_slot_schedule`` and ``check_ring_slot_schedule`` model that
+  S-slot schedule, with the refill either before the wait (two barriers per
+  tile) or after the barrier that publishes the tile (one barrier per tile).
 
 The multiply step uses numpy's matmul on one K slice of integer-valued
 operands, so the model's sum is exact and is compared for equality.
@@ -286,3 +294,92 @@ def check_swap_schedule(trace: list, T: int) -> None:
             computed.append(tile)
     if computed != list(range(T)):
         raise Hazard(f"tiles computed out of order or missing: {computed}")
+
+
+def ring_slot_schedule(T: int, S: int, one_barrier: bool) -> list:
+    """Trace of the S-slot rotate over T K tiles with asynchronous copies.
+
+    The block's threads are taken to move together between barriers.  Events:
+    ``("issue", tile, slot)`` starts the copies of a tile, ``("commit",)``
+    closes a copy group, ``("wait", n)`` returns once at most the newest ``n``
+    groups are still in flight, ``("barrier",)`` is a block barrier and
+    ``("read", tile, slot)`` is the multiply over a tile.
+
+    The prologue fills slots 0..S-2.  Iteration t refills the slot tile t-1
+    used with tile t+S-1 and reads tile t.  With ``one_barrier`` the refill
+    comes after the barrier that publishes tile t (wait S-2 groups, barrier,
+    refill, commit, read); otherwise before the wait (refill, commit, wait
+    S-1 groups, barrier, read, barrier).
+    """
+    trace = []
+    for t in range(S - 1):
+        if t < T:
+            trace.append(("issue", t, t))
+        trace.append(("commit",))
+    cur, nxt = 0, S - 1
+    for t in range(T):
+        if one_barrier:
+            trace += [("wait", S - 2), ("barrier",)]
+            if t + S - 1 < T:
+                trace.append(("issue", t + S - 1, nxt))
+            trace.append(("commit",))
+            trace.append(("read", t, cur))
+        else:
+            if t + S - 1 < T:
+                trace.append(("issue", t + S - 1, nxt))
+            trace += [("commit",), ("wait", S - 1), ("barrier",), ("read", t, cur), ("barrier",)]
+        cur = (cur + 1) % S                      # rotate the slot names
+        nxt = (nxt + 1) % S
+    trace.append(("wait", 0))
+    return trace
+
+
+def check_ring_slot_schedule(trace: list, T: int, S: int) -> None:
+    """Checks the hazards of a ring trace.  A tile is read from the slot it
+    was copied into, after its copy group has been waited for and a barrier
+    has followed (read after write); a slot is refilled only once its
+    previous tile has been read and a barrier has followed that read (write
+    after read); every tile is read once, in order."""
+    groups = []                  # committed copy groups, oldest first: lists of tiles
+    open_group = []
+    landed = {}                  # tile -> barrier epoch in which its group was waited for
+    holds = [None] * S           # tile last copied into each slot
+    read_epoch = [None] * S      # epoch of the last read of each slot's tile
+    unread = [False] * S
+    epoch = 0
+    reads = []
+    for ev in trace:
+        kind = ev[0]
+        if kind == "issue":
+            _, tile, slot = ev
+            if unread[slot]:
+                raise Hazard(f"tile {tile} copied over unread tile {holds[slot]} in slot {slot}")
+            if read_epoch[slot] is not None and read_epoch[slot] >= epoch:
+                raise Hazard(f"tile {tile} copied into slot {slot} with no barrier after the read of "
+                             f"tile {holds[slot]}")
+            holds[slot], unread[slot] = tile, True
+            open_group.append(tile)
+        elif kind == "commit":
+            groups.append(open_group)
+            open_group = []
+        elif kind == "wait":
+            n = ev[1]
+            while len(groups) > n:
+                for tile in groups.pop(0):
+                    landed[tile] = epoch
+        elif kind == "barrier":
+            epoch += 1
+        elif kind == "read":
+            _, tile, slot = ev
+            if holds[slot] != tile:
+                raise Hazard(f"tile {tile} read from slot {slot}, which holds tile {holds[slot]}")
+            if tile not in landed:
+                raise Hazard(f"tile {tile} read before its copy group was waited for")
+            if landed[tile] >= epoch:
+                raise Hazard(f"tile {tile} read with no barrier after its copies landed")
+            read_epoch[slot], unread[slot] = epoch, False
+            reads.append(tile)
+        else:
+            raise ValueError(f"unknown event {ev!r}")
+    if reads != list(range(T)):
+        raise Hazard(f"tiles read out of order or missing: {reads}")

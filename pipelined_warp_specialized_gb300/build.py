@@ -37,8 +37,12 @@ def nvcc() -> str:
 
 
 def _flags(verbose: bool) -> list:
-    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-                "--expt-relaxed-constexpr"]
+    # Hidden visibility: only what a header declares with default visibility
+    # is exported, so two copies of a library in one process keep separate
+    # function-local statics (the compiler would otherwise bind those of
+    # templates process-wide).
+    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE,
+                "-I", CSRC, "--expt-relaxed-constexpr"]
     if verbose:
         f += ["-Xptxas", "-v"]
     return f

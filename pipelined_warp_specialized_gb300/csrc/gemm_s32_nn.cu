@@ -230,10 +230,13 @@ extern "C" int gemm_s32_nn(int64_t M, int64_t N, int64_t K, const int32_t* lhs, 
 // tutorial ch.6 generalises swap(f0, f1) to rotate(f0, f1, f2) for three
 // buffers ("swap：交换的是名称，不是字节"), and the CUDA tutorial ch.4,
 // section 4.8.3 fills S - 1 slots before its main loop.  Here the prologue
-// issues tiles 0 .. S-2; iteration t issues tile t + S - 1 into the slot tile
-// t - 1 vacated, waits until tile t has landed (cp.async.wait_group S - 1,
-// then __syncthreads), multiplies slot t mod S and synchronises again before
-// that slot is refilled.  Rotating the slot index is rotate() over S handles.
+// issues tiles 0 .. S-2; iteration t waits until tile t has landed
+// (cp.async.wait_group, then __syncthreads), issues tile t + S - 1 into the
+// slot tile t - 1 vacated and multiplies slot t mod S.  With S >= 3 the
+// refill follows the barrier that publishes tile t, which also orders it
+// after every read of tile t - 1: one barrier per tile.  With S = 2 the
+// refill is issued before the wait and a second barrier guards the slot.
+// Rotating the slot index is rotate() over S handles.
 // With S tiles in flight the load latency of the small page-size problem is
 // paid about T / (S - 1) times instead of T times; results are bit-identical
 // to the two-buffer kernel (same products, same order, exact arithmetic).
@@ -298,12 +301,30 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, co
     // made the loop execute 60 % more instructions and take twice the cycles
     // on GB300; with S fixed at compile time and the names incremented, the
     // loop is the two-buffer kernel's plus the extra slots in flight.
+    //
+    // With S >= 3 slots the refill of tile t + S - 1 is issued after the
+    // barrier that publishes tile t: that barrier also follows every
+    // thread's reads of tile t - 1, whose slot the refill overwrites, so one
+    // barrier per tile orders both hazards while S - 2 later tiles are still
+    // in flight during the wait.  With two slots that order would leave no
+    // tile in flight during the wait, so S = 2 issues first and
+    // synchronises twice (on the page's 128 x 256 x 256 problem, one barrier
+    // measured 4.2-4.3 us at S = 3..6 against 4.7-4.8 us with two; at S = 2,
+    // 5.2 us against 4.5 us).
+    constexpr bool kOneBarrier = S >= 3;
     int cur = 0, nxt = S - 1;
     for (int t = 0; t < T; ++t) {
-        if (t + S - 1 < T) issue(t + S - 1, nxt);
-        cp_async_commit();
-        cp_async_wait_group<S - 1>();        // tile t has landed ...
-        __syncthreads();                     // ... and is visible to all threads
+        if constexpr (kOneBarrier) {
+            cp_async_wait_group<S - 2>();    // tile t has landed ...
+            __syncthreads();                 // ... is visible, and tile t - 1's slot is free
+            if (t + S - 1 < T) issue(t + S - 1, nxt);
+            cp_async_commit();
+        } else {
+            if (t + S - 1 < T) issue(t + S - 1, nxt);
+            cp_async_commit();
+            cp_async_wait_group<S - 1>();    // tile t has landed ...
+            __syncthreads();                 // ... and is visible to all threads
+        }
         const int32_t* a = As + cur * A_WORDS;
         const int32_t* b = Bs + cur * B_WORDS;
 #pragma unroll
@@ -318,7 +339,7 @@ gemm_s32_nn_ring_kernel(int M, int N, int K, const int32_t* __restrict__ lhs, co
 #pragma unroll
                 for (int j = 0; j < TN; ++j) acc[i][j] += av[i] * bv[j];
         }
-        __syncthreads();                     // slot `cur` is free for tile t + S
+        if constexpr (!kOneBarrier) __syncthreads();   // slot `cur` is free for tile t + S
         cur = cur + 1 == S ? 0 : cur + 1;
         nxt = nxt + 1 == S ? 0 : nxt + 1;
     }

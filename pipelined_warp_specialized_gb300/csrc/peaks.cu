@@ -45,6 +45,8 @@ __global__ void empty_kernel() {
 }  // namespace peaks
 }  // namespace pws
 
+// The library is built with hidden visibility; these three are its exports.
+#pragma GCC visibility push(default)
 extern "C" {
 
 // Multiply-adds per thread: iters * pws_peaks_imad_chains().
@@ -62,3 +64,4 @@ int pws_peaks_empty(int blocks, int threads, cudaStream_t stream) {
 }
 
 }  // extern "C"
+#pragma GCC visibility pop

@@ -24,6 +24,23 @@ def test_exports_every_declared_function(lib):
         assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
 
 
+def test_exports_only_the_declared_functions(lib):
+    # built with hidden visibility, the library's dynamic symbol table holds
+    # exactly the header's functions: no internal function and no
+    # function-local static that a second copy loaded into the same process
+    # could bind to
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm is not installed")
+    out = subprocess.run([nm, "-D", "--defined-only", libbuild.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    syms = {ln.split()[-1]: ln.split()[-2] for ln in out.splitlines() if ln.strip()}
+    assert set(syms) == set(pws.header_functions()), sorted(set(syms) ^ set(pws.header_functions()))
+    assert set(syms.values()) == {"T"}
+
+
 def test_binding_constants_match_the_header():
     # every GEMM_* enumerator the header declares has the same value in the
     # binding, and the binding defines no GEMM_* constant the header lacks

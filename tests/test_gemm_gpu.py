@@ -80,7 +80,7 @@ def test_s32_shapes_bit_exact(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (1, 1, 1), (17, 33, 15), (300, 500, 77), (1000, 1000, 1000),
-                                   (33, 18, 130)])
+                                   (33, 18, 130), (1000, 700, 333)])
 def test_s32_ring_every_stage_count_bit_exact(M, N, K):
     a = inputs.ints(M + 11, 0, (M, K), -1000, 1000)
     b = inputs.ints(N + 13, 1, (K, N), -1000, 1000)
@@ -92,6 +92,37 @@ def test_s32_ring_every_stage_count_bit_exact(M, N, K):
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), want), f"S={s}"
         assert torch.equal(got, two)
+
+
+def test_two_copies_of_the_library_in_one_process(tmp_path):
+    # Each copy of the library keeps its own per-kernel shared-memory
+    # settings, so launches that need more than 48 KB of dynamic shared
+    # memory (the 64 x 64 ring tile at S = 6, every f16 kernel) work from
+    # both copies in turn.
+    import shutil
+    from pipelined_warp_specialized_gb300 import build as libbuild
+    second = str(tmp_path / "libpwsgemm_copy.so")
+    shutil.copy(libbuild.LIB_PATH, second)
+    first = pws.load_library()
+    other = pws.load_library(second)
+    a = inputs.ints(7, 0, (1000, 333), -1000, 1000)
+    b = inputs.ints(8, 1, (333, 700), -1000, 1000)
+    want = oracle.gemm_s32_nn(a, b)
+    da, db = _dev(a), _dev(b)
+    a16 = _dev(inputs.uniform_f16(9, 0, (1024, 1024)))
+    b16 = _dev(inputs.uniform_f16(9, 1, (1024, 1024)))
+    outs = []
+    try:
+        for lib in (other, first, other):
+            pws._lib = lib
+            got = pws.gemm_s32_nn_ring(da, db, stages=6)
+            outs.append(pws.gemm_f16_nt(a16, b16, stages=4))
+            torch.cuda.synchronize()
+            assert pws.gemm_device_status() == pws.GEMM_OK
+            assert np.array_equal(got.cpu().numpy(), want)
+    finally:
+        pws._lib = first
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
 def test_graph_capture_replays_correctly():

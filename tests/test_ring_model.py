@@ -113,3 +113,61 @@ def test_swap_schedule_planted_mistake_is_caught():
     bad2[j] = (phase, act, tile, 1 - buf)
     with pytest.raises(rm.Hazard):
         rm.check_swap_schedule(bad2, 4)
+
+
+@pytest.mark.parametrize("S", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("one_barrier", [False, True])
+def test_ring_slot_schedules_are_hazard_free(S, one_barrier):
+    # both barrier orders of the S-slot rotate read every tile once, in order,
+    # after its copies landed and a barrier followed, and refill a slot only
+    # after a barrier followed the read of its previous tile
+    for T in range(0, 3 * S + 4):
+        rm.check_ring_slot_schedule(rm.ring_slot_schedule(T, S, one_barrier), T, S)
+
+
+def test_ring_slot_schedule_keeps_s_minus_one_tiles_ahead():
+    # the one-barrier order refills after the wait, so during the wait for
+    # tile t only tiles t+1 .. t+S-2 can be in flight; the two-barrier order
+    # has already issued t+S-1 -- which is why it is kept for S = 2, where the
+    # one-barrier order would wait with nothing else in flight
+    for S in (2, 3, 6):
+        for one_barrier, ahead in ((True, S - 2), (False, S - 1)):
+            tr = rm.ring_slot_schedule(4 * S, S, one_barrier)
+            issued, t = 0, 0
+            for ev in tr:
+                if ev[0] == "issue":
+                    issued = max(issued, ev[1] + 1)
+                elif ev[0] == "wait" and t < 4 * S - S:      # steady waits, before the tail runs dry
+                    assert issued - 1 - t == ahead, (S, one_barrier, t, issued)
+                elif ev[0] == "read":
+                    t = ev[1] + 1
+
+
+def test_ring_slot_schedule_planted_mistakes_are_caught():
+    T, S = 10, 4
+    one = rm.ring_slot_schedule(T, S, True)
+    two = rm.ring_slot_schedule(T, S, False)
+    # two-barrier order without its trailing barrier: a slot is refilled in
+    # the interval in which its previous tile is still being read
+    bad = [ev for i, ev in enumerate(two)
+           if not (ev == ("barrier",) and i > 0 and two[i - 1][0] == "read")]
+    with pytest.raises(rm.Hazard, match="no barrier after the read"):
+        rm.check_ring_slot_schedule(bad, T, S)
+    # one-barrier order with every refill moved before its barrier (from
+    # iteration 1 on, the slot refilled still holds the tile read last)
+    bad = list(one)
+    for i in range(1, len(bad)):
+        if bad[i][0] == "issue" and bad[i - 1] == ("barrier",):
+            bad[i - 1], bad[i] = bad[i], bad[i - 1]
+    with pytest.raises(rm.Hazard, match="no barrier after the read"):
+        rm.check_ring_slot_schedule(bad, T, S)
+    # one-barrier order waiting one group too few: the tile is read before it landed
+    bad = [("wait", S - 1) if ev == ("wait", S - 2) else ev for ev in one]
+    with pytest.raises(rm.Hazard, match="before its copy group was waited for"):
+        rm.check_ring_slot_schedule(bad, T, S)
+    # reading the slot the refill targets
+    bad = list(one)
+    j = next(j for j, ev in enumerate(bad) if ev[0] == "read" and ev[1] == 2)
+    bad[j] = ("read", 2, (bad[j][2] + S - 1) % S)
+    with pytest.raises(rm.Hazard):
+        rm.check_ring_slot_schedule(bad, T, S)
