@@ -325,7 +325,9 @@ def per_launch_distribution(pws, torch, stream, shapes=((4096, 4), (8192, 4)), n
         pick = lambda q: us[min(n - 1, int(q * n))]
         out[f"f16_nt_{M}^3/S{S}/per_launch"] = {
             "median_us": round(pick(0.5), 1), "p10_us": round(pick(0.1), 1), "p90_us": round(pick(0.9), 1),
-            "median_TFLOP_s": round(2 * M ** 3 / pick(0.5) / 1e6, 1), "launches": n}
+            "median_TFLOP_s": round(2 * M ** 3 / pick(0.5) / 1e6, 1),
+            "median_frac_of_burst_peak": round(2 * M ** 3 / pick(0.5) / 1e6 / measured_peaks()[0]["bf16_tflops"], 4),
+            "launches": n}
         del a, b, c
     return out
 
@@ -425,11 +427,21 @@ def s32_roofline(torch, stream, us, ops, grid_blocks=128, threads=256):
 
 
 def extra_configs(pws, torch, stream):
-    """Kernel-only timings of every workload (inputs resident); f16 entries
-    carry their fraction of the measured burst dense 16-bit peak."""
+    """Kernel-only timings of every workload (inputs resident).  f16 entries
+    carry their fraction of the measured burst dense 16-bit peak; those timed
+    for 0.25 s of back-to-back launches (at the power limit's steady state)
+    also carry their fraction of the measured sustained peak, the matching
+    denominator for a kernel timed inside a long run."""
     out = {}
     dev = torch.device("cuda")
     burst = measured_peaks()[0]["bf16_tflops"]
+    sustained = measured_peaks()[0]["bf16_tflops_sustained"]
+
+    def fractions(tflops, steady):
+        f = {"frac_of_burst_peak": round(tflops / burst, 4)}
+        if steady:
+            f["frac_of_sustained_peak"] = round(tflops / sustained, 4)
+        return f
     wl = inputs.WORKLOADS["s32_nn_128x256x256"]
     a, b = (torch.from_numpy(x).to(dev) for x in workload_inputs(wl.name))
     c = torch.empty(wl.M, wl.N, dtype=torch.int32, device=dev)
@@ -471,17 +483,17 @@ def extra_configs(pws, torch, stream):
                 res = {"producer": label, "cta_group": plan["cta_group"]}
                 small = wl.flops < 2 ** 34        # launch-bound: time from a CUDA graph
                 for s in wl.stages:
-                    if small and plan["producer"] in (0, 3) and call is pws.gemm_f16_nt:
+                    graph = small and plan["producer"] in (0, 3) and call is pws.gemm_f16_nt
+                    if graph:
                         ms = time_graph(lambda st: call(a, b, c, stages=s, stream=st), torch)
                     else:
                         ms = time_steady(lambda: call(a, b, c, stages=s, stream=stream), torch, stream)
                     ps = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), s)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
-                                    "frac_of_burst_peak": round(wl.flops / ms / 1e9 / burst, 4),
+                                    **fractions(wl.flops / ms / 1e9, not graph),
                                     "GB_s": round((wl.M * wl.K + wl.N * wl.K + wl.M * wl.N) * 2 / ms / 1e6, 1),
                                     "tile": f"{ps['bm']}x{ps['bn']}"}
-                    res[f"S{s}"]["timing"] = ("CUDA-graph replay"
-                                              if small and plan["producer"] in (0, 3) and call is pws.gemm_f16_nt
+                    res[f"S{s}"]["timing"] = ("CUDA-graph replay" if graph
                                               else "0.25 s warm-up, then 0.25 s of back-to-back launches")
             finally:
                 pws.gemm_set_debug_flags(0)
@@ -501,7 +513,7 @@ def extra_configs(pws, torch, stream):
                 for s in range(1, 7):
                     ms = time_steady(lambda: pws.gemm_f16_nt(a, b, c, stages=s, stream=stream), torch, stream)
                     res[f"S{s}"] = {"us": round(ms * 1e3, 1), "TFLOP_s": round(wl.flops / ms / 1e9, 1),
-                                    "frac_of_burst_peak": round(wl.flops / ms / 1e9 / burst, 4),
+                                    **fractions(wl.flops / ms / 1e9, True),
                                     "tile": "256x256",
                                     "timing": "0.25 s warm-up, then 0.25 s of back-to-back launches"}
                 plan_n = pws.gemm_f16_nt_plan(wl.M, wl.N, wl.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), 6)
