@@ -398,7 +398,38 @@ def peaks_library():
     lib.pws_peaks_empty.argtypes = [i32, i32, vp]
     lib.pws_peaks_empty.restype = i32
     lib.pws_peaks_imad_chains.restype = i32
+    lib.pws_peaks_mma.argtypes = [i32, i32, ctypes.c_uint64, vp, vp, vp]
+    lib.pws_peaks_mma.restype = i32
+    lib.pws_peaks_mma_step_flops.restype = ctypes.c_longlong
     return lib
+
+
+def tensor_rate(torch, stream, steps=8192):
+    """The tensor pipe's dense f16 -> fp32 rate per SM per clock, measured:
+    one CTA per SM issues `steps` K steps of four tcgen05.mma (M = 128,
+    N = 256, K = 16) back to back from shared memory, timed in SM cycles
+    (clock64) from the first issue to the last MMA's completion; the median
+    over the CTAs of the second of two launches."""
+    lib = peaks_library()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = torch.zeros(2 * sms, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        rc = lib.pws_peaks_mma(sms, steps, 2_000_000_000, out.data_ptr(), status.data_ptr(), stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"pws_peaks_mma failed ({rc})")
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("pws_peaks_mma: a bounded wait gave up")
+    v = out.cpu().numpy().reshape(sms, 2).astype(np.float64)
+    flops = steps * lib.pws_peaks_mma_step_flops()
+    per_clk = np.median(flops / v[:, 0])
+    ghz = np.median(v[:, 0] / v[:, 1])
+    return {"flop_per_clk_per_sm": round(float(per_clk), 1), "sms": sms,
+            "sm_ghz_during": round(float(ghz), 3),
+            "how": f"{sms} CTAs x {steps} K steps of 4 tcgen05.mma.cta_group::1.kind::f16 "
+                   "(128 x 256 x 16) from one shared-memory tile pair, SM cycles from the first issue "
+                   "to the last completion, median over CTAs"}
 
 
 def s32_roofline(torch, stream, us, ops, grid_blocks=128, threads=256):
@@ -643,6 +674,23 @@ def run_ours(args, world, rank, local):
                                "(f16 and bf16 share the tensor rate)",
                 "traffic": profiled_traffic(M, N, K, S),
                 "algorithmic_bytes_per_launch": int((M * K + N * K + M * N) * 2)}
+    # the tensor pipe's own ceiling: SMs x the measured dense f16 flops per
+    # SM per clock x a clock -- the SM's maximum, and the clock the
+    # microbenchmark itself ran at with every tensor pipe busy (the power
+    # limit lowers it).  The clock samples of the timed region are not used:
+    # at 50 ms apart they mostly fall outside a region this short.
+    try:
+        pipe = tensor_rate(torch, stream)
+        at = pipe["sms"] * pipe["flop_per_clk_per_sm"] * pipe["sm_ghz_during"] * 1e9 / 1e12
+        pipe.update({"ceiling_tflops_at_its_clock": round(at, 1),
+                     "frac_of_ceiling_at_its_clock": round(achieved / at, 4)})
+        if clocks and clocks.get("sm_max_mhz"):
+            top = pipe["sms"] * pipe["flop_per_clk_per_sm"] * clocks["sm_max_mhz"] * 1e6 / 1e12
+            pipe.update({"ceiling_tflops_at_max_clock": round(top, 1),
+                         "frac_of_ceiling_at_max_clock": round(achieved / top, 4)})
+    except (OSError, RuntimeError) as ex:
+        pipe = {"unavailable": str(ex)}
+    roofline["tensor_pipe"] = pipe
 
     extras = None
     if rank == 0 and world == 1 and not args.no_sweep and (M, N, K) == (8192, 8192, 8192) and args.tile == "auto":
