@@ -191,6 +191,74 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (the
+    driver's management library, read-only queries) every `interval_ms`
+    from a background thread, so that even a timed region of a few
+    milliseconds holds samples; the same output as ClockSampler.  These are
+    the values the driver reports, as nvidia-smi does: on GB300 they follow
+    the load with a lag (the power reading is a window average), so within
+    a region of tens of milliseconds they show at most the start of the
+    power limit's effect."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch, device: int, interval_ms: float = 2.0):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(device), "uuid", None)
+        ok = False
+        if uuid is not None:
+            ok = self.lib.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(device, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.interval = interval_ms / 1e3
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _one(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        t = time.time()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:       # NVML_CLOCK_SM
+            return
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        self.samples.append((t, mhz.value, mw.value / 1e3, rs.value))
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            self._one()
+            time.sleep(self.interval)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        time.sleep(0.05)
+
+    def stop(self, t0, t1):
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        top = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(top))
+        self.lib.nvmlShutdown()
+        rows = [x for x in self.samples if t0 <= x[0] <= t1]
+        reasons = sorted({name for _, _, _, r in rows for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median([r[1] for r in rows]) if rows else None,
+                "sm_mhz_min": min(r[1] for r in rows) if rows else None,
+                "sm_max_mhz": top.value or None,
+                "power_w_median": round(statistics.median([r[2] for r in rows]), 1) if rows else None,
+                "reasons": reasons, "samples": len(rows),
+                "source": f"NVML every {self.interval * 1e3:.0f} ms inside the timed region"}
+
+
 # ---------------------------------------------------------------- our arm
 
 def time_launches(fn, steps, warmup, torch, stream):
@@ -614,7 +682,12 @@ def run_ours(args, world, rank, local):
     if status != pws.GEMM_OK:
         raise RuntimeError(f"device status after warm-up: {pws.gemm_status_string(status)}")
 
-    sampler = ClockSampler(local) if not args.no_clocks else None
+    sampler = None
+    if not args.no_clocks:
+        try:
+            sampler = NvmlSampler(torch, local)
+        except (OSError, AttributeError):
+            sampler = ClockSampler(local)          # nvidia-smi, 50 ms apart
     if sampler:
         sampler.start()
     if world > 1:
@@ -676,9 +749,11 @@ def run_ours(args, world, rank, local):
                 "algorithmic_bytes_per_launch": int((M * K + N * K + M * N) * 2)}
     # the tensor pipe's own ceiling: SMs x the measured dense f16 flops per
     # SM per clock x a clock -- the SM's maximum, and the clock the
-    # microbenchmark itself ran at with every tensor pipe busy (the power
-    # limit lowers it).  The clock samples of the timed region are not used:
-    # at 50 ms apart they mostly fall outside a region this short.
+    # microbenchmark itself ran at (cycles over nanoseconds, in the kernel)
+    # right after the timed region, with every tensor pipe busy: the power
+    # limit lowers it.  The driver's clock readings are not used here: they
+    # lag a load of milliseconds (2070 MHz and under 200 W read during a
+    # region the microbenchmark then ran at 1.55 GHz)
     try:
         pipe = tensor_rate(torch, stream)
         at = pipe["sms"] * pipe["flop_per_clk_per_sm"] * pipe["sm_ghz_during"] * 1e9 / 1e12
@@ -688,6 +763,7 @@ def run_ours(args, world, rank, local):
             top = pipe["sms"] * pipe["flop_per_clk_per_sm"] * clocks["sm_max_mhz"] * 1e6 / 1e12
             pipe.update({"ceiling_tflops_at_max_clock": round(top, 1),
                          "frac_of_ceiling_at_max_clock": round(achieved / top, 4)})
+
     except (OSError, RuntimeError) as ex:
         pipe = {"unavailable": str(ex)}
     roofline["tensor_pipe"] = pipe
