@@ -350,7 +350,7 @@ int gemm_set_scratch_pool(int enable);
  * arguments, without touching a device (host logic only).  Validates the
  * arguments exactly as gemm_f16_nt does and returns the same status.
  *   plan[0] tile rows per CTA group (BM)      plan[1] tile columns (BN)
- *   plan[2] K per ring slot (64; 192 or 128 for multi-box slots)
+ *   plan[2] K per ring slot (64; 256, 192 or 128 for multi-box slots)
  *   plan[3] CTAs per tile (1 or 2)
  *   plan[4] producer: 0 = tensor memory accelerator, 1 = async copy,
  *           2 = tensor memory accelerator on an aligned copy (in the fixed

@@ -161,12 +161,16 @@ struct Shape {
 
 // Shared-memory carve-up (offsets from a 1024-byte aligned base).  A slot
 // holds KB 64-wide K boxes of each operand: slot s holds A box j at
-// A + s * A_STRIDE + j * A_SLOT and B box j at B + s * B_STRIDE + j * B_SLOT,
+// A + s * A_STRIDE + j * A_SLOT and B box j at B + s * B_STRIDE + j * B_BOX,
 // or, for the wide tile (KB = 1), its NW B boxes at B + s * B_STRIDE + h * B_SLOT.
+// KB = 4 serves half-width units only (every unit of the launch is one):
+// their B boxes are 64 rows, half a B_SLOT, so four boxes of each operand fit
+// where three full ones would.
 template <int S, int NW = 1, int KB = 1>
 struct Layout {
+    static constexpr int B_BOX = KB == 4 ? B_SLOT / 2 : B_SLOT;
     static constexpr int A_STRIDE = KB * A_SLOT;
-    static constexpr int B_STRIDE = NW * KB * B_SLOT;
+    static constexpr int B_STRIDE = NW * KB * B_BOX;
     static constexpr int A = 0;
     static constexpr int B = S * A_STRIDE;
     static constexpr int EPI = S * (A_STRIDE + B_STRIDE);
@@ -603,9 +607,11 @@ __device__ void realign_producer(const Params& p, const Waiter& W, uint32_t sA, 
 // every producer with one bound; a CTA pair has a kernel per producer kind,
 // so the TMA one keeps the registers eight producer warps would take.
 //
-// KB = 2 or 3 (single-CTA tile, TMA): each slot holds KB 64-wide K boxes of
-// each operand, so a latency-bound K loop runs 1/KB as many slot round
-// trips; the multiplies keep their K order, so the result bits do not change.
+// KB = 2, 3 or 4 (single-CTA tile, TMA): each slot holds KB 64-wide K boxes
+// of each operand, so a latency-bound K loop runs 1/KB as many slot round
+// trips; the multiplies keep their K order, so the result bits do not
+// change.  KB = 4 is for launches whose units are all half-width (the B
+// boxes are half size).
 template <int CG, int S, int NW, int PK, int KB = 1>
 __global__ void __launch_bounds__(((CG == 1 || PK == 1 ? COPY_WARPS : 1) + 1 + epi_warps<NW, PK>()) * 32, 1)
 gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -729,7 +735,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                             mbar_arrive_expect_tx(bFULL + 8 * stage, static_cast<uint32_t>(nk) * bytes);
                             for (int j = 0; j < nk; ++j) {
                                 tma_load_2d(a_dst + j * A_SLOT, &tmA, (kb * KB + j) * BK, m_cta, bFULL + 8 * stage);
-                                tma_load_2d(b_dst + j * B_SLOT, tb, (kb * KB + j) * BK, n_cta, bFULL + 8 * stage);
+                                tma_load_2d(b_dst + j * L::B_BOX, tb, (kb * KB + j) * BK, n_cta, bFULL + 8 * stage);
                             }
                         } else if constexpr (CG == 1) {
                             mbar_arrive_expect_tx(bFULL + 8 * stage, bytes);
@@ -837,7 +843,7 @@ gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                                 // a box wholly past K was not loaded (two-box slots)
                                 if (KB > 1 && ((kb + j) * KB + bx) * BK >= p.K) break;
                                 const uint64_t adesc = make_sdesc(sA + st[j] * L::A_STRIDE + bx * A_SLOT);
-                                const uint64_t bdesc = make_sdesc(sB + st[j] * L::B_STRIDE + bx * B_SLOT);
+                                const uint64_t bdesc = make_sdesc(sB + st[j] * L::B_STRIDE + bx * L::B_BOX);
 #pragma unroll
                                 for (int k = 0; k < BK / UMMA_K; ++k) {
                                     // +32 bytes of K per step: +2 in the (address >> 4) field
@@ -1395,7 +1401,7 @@ struct Plan {
     int tiles_m = 0, tiles_n = 0, num_tiles = 0, num_kb = 0;
     int smem = 0;
     int ksplit = 1;             // 2: two CTAs (a cluster) per single-CTA tile, one K half each
-    int kb = 1;                 // 64-wide K boxes per ring slot (2 or 3: single-CTA TMA tile, S <= 3)
+    int kb = 1;                 // 64-wide K boxes per ring slot (2, 3 or 4: single-CTA TMA tile, S <= 3)
 };
 
 // Fewest K blocks for which small single-CTA GEMMs split K over two CTAs.
@@ -1409,6 +1415,7 @@ constexpr int64_t kPooledRowAlign = 64;
 constexpr int WIDE_MAX_STAGES = 4;
 
 int smem_for(int stages, int nw, int kb = 1) {
+    if (kb == 4) return stages == 1 ? Layout<1, 1, 4>::DYN : Layout<2, 1, 4>::DYN;
     if (kb == 3) return stages == 1 ? Layout<1, 1, 3>::DYN : Layout<2, 1, 3>::DYN;
     if (kb == 2) return Layout<3, 1, 2>::DYN;
     if (nw == 2) {
@@ -1557,12 +1564,22 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, const void* lhs, const void* rhs
     // Multi-box slots: on the single-CTA TMA tile with up to three slots,
     // when the tiles fit in one wave, so that each CTA's chain of K blocks
     // through the ring is what bounds the call: three boxes per slot for one
-    // or two slots, two for three (the most that fit in shared memory).
-    // Each element keeps its K order: the result is the same for every choice.
+    // or two slots, two for three (the most that fit in shared memory).  When
+    // every tile runs as two half-width units (the tail split of a launch
+    // whose tiles fill at most half the SMs: the rule of run_plan, whose
+    // grid for this tile is one CTA per SM), their half-size B boxes let one
+    // or two slots hold four boxes.  Measured on GB300 (graph replay),
+    // 1024^3 at S = 2 / 1: 6.46 / 9.05 us with three boxes, 6.25 / 8.30 us
+    // with four; 1024 x 1024 x 512 at S = 2 the same either way.  Each
+    // element keeps its K order: the result is the same for every choice.
     if (pl.cg == 1 && pl.ksplit == 1 && pl.producer == kProducerTma && stages <= 3 && pl.num_kb >= 2 &&
         !(flags & GEMM_DEBUG_NO_DOUBLE_SLOT) &&
-        ((flags & GEMM_DEBUG_FORCE_DOUBLE_SLOT) || pl.num_tiles <= num_sms))
+        ((flags & GEMM_DEBUG_FORCE_DOUBLE_SLOT) || pl.num_tiles <= num_sms)) {
         pl.kb = stages <= 2 ? 3 : 2;
+        if (stages <= 2 && !(flags & (GEMM_DEBUG_NO_SPLIT | GEMM_DEBUG_FORCE_DOUBLE_SLOT)) &&
+            2 * pl.num_tiles <= num_sms)
+            pl.kb = 4;
+    }
     pl.num_kb = static_cast<int>((K + BK * pl.kb - 1) / (BK * pl.kb));
     pl.smem = smem_for(stages, pl.nw, pl.kb);
     return pl;
@@ -1634,6 +1651,7 @@ inline int pk_of(const Plan& pl) { return pl.cg == 2 && pl.producer != kProducer
 
 int capacity_of(const Plan& pl, int stages, const DeviceInfo& info) {
     const int threads = block_threads(pl);
+    if (pl.kb == 4) return stages == 1 ? capacity<1, 1, 1, 0, 4>(info, threads) : capacity<1, 2, 1, 0, 4>(info, threads);
     if (pl.kb > 1) {
         switch (stages) {
             case 1: return capacity<1, 1, 1, 0, 3>(info, threads);
@@ -1699,6 +1717,13 @@ int launch_stages(int stages, const Plan& pl, const DeviceInfo& info, const CUte
 
 int launch_plan(int stages, const Plan& pl, const DeviceInfo& info, const CUtensorMap& ta, const CUtensorMap& tb,
                 const CUtensorMap& tbh, const CUtensorMap& tc, const Params& p, cudaStream_t stream) {
+    if (pl.kb == 4) {
+        // half-size B boxes: only a launch of half-width units may use them
+        if (p.split != 2 || p.full_units != 0) return GEMM_ERR_LAUNCH;
+        if (stages == 1) return launch<1, 1, 1, 0, 4>(pl, info, ta, tb, tbh, tc, p, stream);
+        if (stages == 2) return launch<1, 2, 1, 0, 4>(pl, info, ta, tb, tbh, tc, p, stream);
+        return GEMM_ERR_UNSUPPORTED_STAGES;
+    }
     if (pl.kb > 1) {
         switch (stages) {
             case 1: return launch<1, 1, 1, 0, 3>(pl, info, ta, tb, tbh, tc, p, stream);

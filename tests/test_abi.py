@@ -222,11 +222,14 @@ def test_plan_sum_order_never_depends_on_stages(lib):
                 assert len({(p["cta_group"], p["k_split"]) for p in plans}) == 1, (M, N, K)
                 for s, p in enumerate(plans, start=1):
                     assert p["bn"] != 512 or s <= 4, (M, N, K, s)            # the wide tile needs <= 4 slots
-                    # multi-box slots (192 or 128 K columns per slot,
-                    # multiplied in the same K order) only on the single-CTA
-                    # tile, without the K split, with at most 3 slots
-                    assert p["bk"] == 64 or (p["bk"] == (192 if s <= 2 else 128) and s <= 3
+                    # multi-box slots (192 or 256 K columns per slot for at
+                    # most 2 slots, 128 for 3, multiplied in the same K
+                    # order) only on the single-CTA tile, without the K split;
+                    # four boxes only where every tile runs as two half-width
+                    # units (the tiles fill at most half the SMs)
+                    assert p["bk"] == 64 or (p["bk"] in ((192, 256) if s <= 2 else (128,)) and s <= 3
                                              and p["cta_group"] == 1 and p["k_split"] == 1), (M, N, K, s)
+                    assert p["bk"] != 256 or 2 * p["tiles"] <= 152, (M, N, K, s)
                     assert p["k_blocks"] == -(-K // p["bk"]), (M, N, K, s)
                     assert p["k_split"] == 1 or p["cta_group"] == 1, (M, N, K)
                     assert p["k_split"] == 1 or p["k_blocks"] >= 32, (M, N, K)

@@ -216,7 +216,7 @@ def test_f16_stage_counts_bitwise_identical(flags):
     (2560, 2560, 256),      # wide tile for S <= 2, 256 x 256 for S >= 3: the same bits
     (2048, 2048, 512),      # the pair tile by wave count (64 pair tiles against 256 single)
     (1024, 1152, 2100),     # the K split, the operands read in place
-    (1024, 1024, 1024),     # multi-box slots (192 / 128 K columns) for S <= 3, one box for S >= 4
+    (1024, 1024, 1024),     # multi-box slots (256 / 128 K columns) for S <= 3, one box for S >= 4
     (700, 900, 1000),       # multi-box slots, the last slot's later boxes past K (K = 1000)
     (300, 260, 136),        # multi-box slots, the last slot's last box partly inside K
 ])
@@ -486,6 +486,31 @@ def test_f16_two_box_slots_bitwise_equal_one_box(M, N, K, S, extra):
     assert bk == (64 if K <= 64 else (192 if S <= 2 else 128))
     outs = [run_f16(a, b, S, f | extra) for f in (pws.GEMM_DEBUG_FORCE_DOUBLE_SLOT, pws.GEMM_DEBUG_NO_DOUBLE_SLOT)]
     assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert_f16_ok(outs[0], oracle.gemm_f16_nt_f64(a, b), K)
+
+
+@pytest.mark.parametrize("M,N,K,S,extra", [
+    (1024, 1024, 1024, 2, 0),   # the 1024^3 workload: 128 half-width units, 4 slots of 4 boxes
+    (1024, 1024, 1024, 1, 0),
+    (700, 900, 1000, 2, 0),     # the last slot's last box partly inside K
+    (300, 260, 136, 2, 0),      # one slot: three boxes inside K, the fourth past it
+    (1000, 1100, 1090, 2, POOL),    # TMA on the repacked copy
+])
+def test_f16_four_box_slots_bitwise_equal_one_and_three_boxes(M, N, K, S, extra):
+    # where every tile runs as two half-width units, their half-size B boxes
+    # let a slot hold four boxes of each operand: the K order, and so the
+    # bits, stay those of one and of three boxes per slot
+    a = inputs.uniform_f16(91, 0, (M, K))
+    b = inputs.uniform_f16(91, 1, (N, K))
+    pws.gemm_set_scratch_pool(bool(extra & POOL))
+    try:
+        assert pws.gemm_f16_nt_plan(M, N, K, stages=S)["bk"] == 256
+    finally:
+        pws.gemm_set_scratch_pool(False)
+    outs = [run_f16(a, b, S, f | extra)
+            for f in (0, pws.GEMM_DEBUG_FORCE_DOUBLE_SLOT, pws.GEMM_DEBUG_NO_DOUBLE_SLOT)]
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint16), outs[0].view(np.uint16))
     assert_f16_ok(outs[0], oracle.gemm_f16_nt_f64(a, b), K)
 
 
