@@ -62,7 +62,7 @@
 // memory is touched only once that grid has completed.
 //
 // Every wait is bounded (wait_timeout_ns); a role that gives up records a
-// timeout in the library's status word, raises a CTA-local abort flag that
+// timeout in the status word of the call's stream, raises a CTA-local abort flag that
 // the other roles poll, and every role then runs the common exit path, so
 // the kernel always returns.  Waits that last about one K block (the ring's)
 // count the limit from their start; the waits that last a whole K loop (a
