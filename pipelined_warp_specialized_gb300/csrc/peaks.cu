@@ -161,12 +161,15 @@ long long pws_peaks_mma_step_flops() {
 int pws_peaks_mma(int blocks, int steps, unsigned long long timeout_ns, unsigned long long* out, unsigned* status,
                   cudaStream_t stream) {
     if (blocks <= 0 || steps <= 0 || !out || !status) return 1;
-    static bool configured = false;
-    if (!configured) {
+    // the shared-memory limit is a per-device setting of the kernel
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= 64) return 5;
+    static bool configured[64] = {};
+    if (!configured[device]) {
         if (cudaFuncSetAttribute(pws::peaks::mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  pws::peaks::kMmaSmem) != cudaSuccess)
             return 5;
-        configured = true;
+        configured[device] = true;
     }
     pws::peaks::mma_kernel<<<blocks, 128, pws::peaks::kMmaSmem, stream>>>(steps, timeout_ns, out, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 5;
