@@ -604,6 +604,30 @@ def _sampled_entries(M, N, seed, n_random, tile=128):
     return np.concatenate(rr), np.concatenate(cc)
 
 
+@pytest.mark.parametrize("M,N,K,S", [
+    (1, 8192, 4096, 4),       # one output row: a single-CTA tile row, the K split
+    (8192, 1, 4096, 4),       # one output column
+    (65536, 128, 256, 3),     # tall: 512 single tiles or 256 pair tiles, several waves
+    (128, 65536, 256, 2),     # wide: the same, transposed
+    (33, 40000, 72, 1),       # one slot, a ragged single K block past 64
+    (40000, 33, 1000, 6),     # six slots on the pair tile with one ragged column tile
+    (2, 3, 70000, 2),         # long K on one tile: the K split, 1094 K blocks
+])
+def test_f16_extreme_aspect_ratios(M, N, K, S):
+    # shapes at the edges of the plan's rules, against the f64 oracle on
+    # whole rows and columns crossing every tile plus random entries, and
+    # bitwise equal at another ring depth
+    a = inputs.uniform_f16(M % 997 + 3, 0, (M, K))
+    b = inputs.uniform_f16(N % 991 + 5, 1, (N, K))
+    got = run_f16(a, b, S)
+    other = run_f16(a, b, 1 if S != 1 else 3)
+    assert np.array_equal(got.view(np.uint16), other.view(np.uint16))
+    rows, cols = _sampled_entries(M, N, 7, 3000)
+    ref = oracle.gemm_f16_nt_entries(a, b, rows, cols)
+    res = oracle.check_f16(got[rows, cols], ref, K)
+    assert res["ok"], res
+
+
 def test_f16_4096_config_full():
     # every one of the 16.8 M outputs against the f64 oracle (about 3 s on 16 host cores)
     wl = inputs.WORKLOADS["f16_nt_4096"]
